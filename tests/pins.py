@@ -1,0 +1,294 @@
+"""Pins of the CPU oracle: checks against what the pages and the mathematics fix.
+
+Each pin takes one compiled copy of the oracle (so the mutant tests can run the
+same pins on copies with a planted mistake) and raises AssertionError when the
+copy disagrees with:
+  - the hand-built words under tests/golden/ (e2m1 table, int4 nibble - 8,
+    int3 dual planes, int8 bytes), each fixture citing its passage;
+  - IEEE f32 multiplication (numpy) for the f32 dequantized weight;
+  - an independent dense evaluation (codes packed by the tests' own packer,
+    numpy f64 matmul) for the GEMV, gate/up and the expert group;
+  - closed forms: zero-scale groups give exact zeros, linearity in x, exact
+    integer results for small-integer x and power-of-two scales, silu against
+    scipy's logistic function, invariants of the routed sum (one-hot weights,
+    zero weights, permuted ranks, repeated experts).
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+from scipy.special import expit
+
+from packing import (ALL_FMTS, INT3_G64, INT4_G, INT8_ROW, MXFP4_G32, dense, e2m1_table,
+                     group_of, load_table, pack, random_codes, values_of)
+
+
+def _close(a, b, rtol=1e-12, atol=0.0):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    scale = max(np.abs(b).max(), 1e-300)
+    err = np.abs(a - b).max() / scale if a.size else 0.0
+    assert err <= rtol or np.allclose(a, b, rtol=rtol, atol=atol), f"max rel err {err:.3e} > {rtol:.1e}"
+
+
+# --- step a1/a2: codes and values on hand-built words -----------------------
+
+def pin_e2m1(orc):
+    tab = e2m1_table()
+    for c in range(16):
+        v = orc.e2m1(c)
+        assert v == tab[c] and np.signbit(v) == np.signbit(tab[c]), f"e2m1 code {c:#x}: {v} != {tab[c]}"
+        v = orc.code_value(MXFP4_G32, c)
+        assert v == tab[c] and np.signbit(v) == np.signbit(tab[c])
+    # every code through the packed path: byte b holds codes (b & 15, b >> 4)
+    codes = np.array([[c for c in range(16)] * 2], dtype=np.int64)
+    got = orc.codes(MXFP4_G32, pack(MXFP4_G32, codes), 1, 32)
+    assert np.array_equal(got, codes)
+
+
+def pin_int4_nibbles(orc):
+    rows = load_table("int4_nibbles.txt")
+    for byte_s, v_even, v_odd in rows:
+        byte = int(byte_s, 16)
+        for o, b in ((0, 0), (1, 5)):          # row 1, byte 5 -> inputs 10, 11
+            w = np.full(2 * 16, 0x88, dtype=np.uint8)  # 2 rows x 32 inputs
+            w[o * 16 + b] = byte
+            c0 = orc.codes(INT4_G, w, 2, 32)[o, 2 * b]
+            c1 = orc.codes(INT4_G, w, 2, 32)[o, 2 * b + 1]
+            assert orc.code_value(INT4_G, int(c0)) == int(v_even), (byte_s, c0)
+            assert orc.code_value(INT4_G, int(c1)) == int(v_odd), (byte_s, c1)
+
+
+def pin_int3_planes(orc):
+    O, I = 2, 64
+    for r in load_table("int3_planes.txt"):
+        A0, A1, B = (int(v, 16) for v in r[:3])
+        want = [int(v) for v in r[3:]]
+        w = np.zeros(O * I // 4 + O * I // 8, dtype=np.uint8)
+        w[1 * 16 + 0] = A0                       # row 1, plane A bytes 0, 1
+        w[1 * 16 + 1] = A1
+        w[O * I // 4 + 1 * 8 + 0] = B           # plane B after the whole plane A
+        got = orc.codes(INT3_G64, w, O, I)
+        assert list(got[1, :8]) == want, (r, list(got[1, :8]))
+        assert not got[0].any() and not got[1, 8:].any()
+        for c, v in zip(want, got[1, :8]):
+            assert orc.code_value(INT3_G64, int(v)) == c - 4
+    # every code at every position of both rows
+    for o in range(O):
+        for p in range(I):
+            for c in range(8):
+                codes = np.zeros((O, I), dtype=np.int64)
+                codes[o, p] = c
+                w = np.zeros(O * I // 4 + O * I // 8, dtype=np.uint8)
+                w[o * 16 + p // 4] |= (c & 3) << (2 * (p % 4))
+                w[O * I // 4 + o * 8 + p // 8] |= ((c >> 2) & 1) << (p % 8)
+                if p % 16 == 0 or c == 7:
+                    assert np.array_equal(orc.codes(INT3_G64, w, O, I), codes), (o, p, c)
+
+
+def pin_int8_bytes(orc):
+    for byte_s, v in load_table("int8_bytes.txt"):
+        w = np.zeros(2 * 16, dtype=np.uint8)
+        w[16 + 3] = int(byte_s, 16)
+        got = orc.codes(INT8_ROW, w, 2, 16)
+        assert got[1, 3] == int(v) and orc.code_value(INT8_ROW, int(got[1, 3])) == int(v)
+
+
+def pin_random_codes(orc):
+    rng = np.random.default_rng(7)
+    for fmt in ALL_FMTS:
+        codes = random_codes(fmt, 3, 128, rng)
+        got = orc.codes(fmt, pack(fmt, codes), 3, 128)
+        assert np.array_equal(got, codes), f"fmt {fmt}"
+
+
+# --- step a2: f32 dequantized weights ----------------------------------------
+
+def pin_dequant_f32(orc):
+    rng = np.random.default_rng(11)
+    for fmt in ALL_FMTS:
+        for gs_req in (None, 64, 128):
+            O, I = 3, 256
+            gs = group_of(fmt, I, gs_req)
+            if fmt in (INT3_G64, MXFP4_G32, INT8_ROW) and gs_req is not None:
+                continue
+            codes = random_codes(fmt, O, I, rng)
+            scales = rng.lognormal(-4, 3.0, size=O * (I // gs)).astype(np.float32)
+            scales[0] = np.float32(1e-41)      # subnormal scale
+            scales[-1] = np.float32(1e36)       # large, no f32 overflow at |value| <= 128
+            got = orc.dequant_f32(fmt, gs, pack(fmt, codes), scales, O, I)
+            want = values_of(fmt, codes).astype(np.float32) * np.repeat(scales.reshape(O, -1), gs, axis=1)
+            assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32)), f"fmt {fmt} gs {gs}"
+
+
+# --- step a3: the GEMV -------------------------------------------------------
+
+def pin_gemv_bruteforce(orc):
+    rng = np.random.default_rng(13)
+    for fmt in ALL_FMTS:
+        for gs_req in (None, 64):
+            for s in (1, 4):
+                O, I = 4, 64 if gs_req is None else 128
+                gs = group_of(fmt, I, gs_req)
+                if gs_req is not None and fmt != INT4_G:
+                    continue
+                codes = random_codes(fmt, O, I, rng)
+                scales = rng.lognormal(-4, 0.5, size=O * (I // gs)).astype(np.float32)
+                x = rng.standard_normal((s, I)).astype(np.float32)
+                got = orc.qgemv(fmt, gs, pack(fmt, codes), scales, x, O, I)
+                want = x.astype(np.float64) @ dense(fmt, codes, scales, gs).T
+                _close(got, want)
+                # scale 1: a plain dense matvec of the code values
+                ones = np.ones(O * (I // gs), dtype=np.float32)
+                got1 = orc.qgemv(fmt, gs, pack(fmt, codes), ones, x, O, I)
+                _close(got1, x.astype(np.float64) @ values_of(fmt, codes).T)
+                rows = np.array([3, 0, 2])
+                _close(orc.qgemv_rows(fmt, gs, pack(fmt, codes), scales, x, O, I, rows), got[:, rows])
+
+
+def pin_zero_scales(orc):
+    rng = np.random.default_rng(17)
+    for fmt in ALL_FMTS:
+        O, I = 3, 128
+        gs = group_of(fmt, I)
+        codes = random_codes(fmt, O, I, rng)
+        x = rng.standard_normal((2, I)).astype(np.float32)
+        zero = np.zeros(O * (I // gs), dtype=np.float32)
+        assert not orc.qgemv(fmt, gs, pack(fmt, codes), zero, x, O, I).any()
+        if gs < I:
+            scales = rng.lognormal(-4, 0.5, size=O * (I // gs)).astype(np.float32)
+            scales.reshape(O, -1)[:, 1] = 0.0        # group 1 of every row is zero
+            y1 = orc.qgemv(fmt, gs, pack(fmt, codes), scales, x, O, I)
+            codes2 = codes.copy()
+            codes2[:, gs:2 * gs] = random_codes(fmt, O, gs, rng)
+            y2 = orc.qgemv(fmt, gs, pack(fmt, codes2), scales, x, O, I)
+            assert np.array_equal(y1, y2), f"fmt {fmt}: a zero-scale group changed y"
+
+
+def pin_linearity(orc):
+    rng = np.random.default_rng(19)
+    for fmt in ALL_FMTS:
+        O, I = 4, 128
+        gs = group_of(fmt, I)
+        w = pack(fmt, random_codes(fmt, O, I, rng))
+        scales = rng.lognormal(-4, 0.5, size=O * (I // gs)).astype(np.float32)
+        x1 = rng.standard_normal(I).astype(np.float32)
+        x2 = rng.standard_normal(I).astype(np.float32)
+        x1[1::2] = 0.0                              # disjoint supports: a*x1 + b*x2 exact in f32
+        x2[0::2] = 0.0
+        a, b = np.float32(0.25), np.float32(-8.0)
+        x3 = a * x1 + b * x2
+        y1 = orc.qgemv(fmt, gs, w, scales, x1, O, I)
+        y2 = orc.qgemv(fmt, gs, w, scales, x2, O, I)
+        y3 = orc.qgemv(fmt, gs, w, scales, x3, O, I)
+        _close(y3, float(a) * y1 + float(b) * y2, rtol=1e-12)
+
+
+def pin_integer_exact(orc):
+    rng = np.random.default_rng(23)
+    for fmt in ALL_FMTS:
+        O, I = 3, 256
+        gs = group_of(fmt, I)
+        codes = random_codes(fmt, O, I, rng)
+        k = rng.integers(-8, 1, size=O * (I // gs))
+        scales = np.ldexp(np.ones(k.size), k).astype(np.float32)
+        x = rng.integers(-4, 5, size=(2, I)).astype(np.float32)
+        got = orc.qgemv(fmt, gs, pack(fmt, codes), scales, x, O, I)
+        vals = values_of(fmt, codes)
+        for t in range(2):
+            for o in range(O):
+                exact = sum(Fraction(vals[o, i]) * Fraction(2) ** int(k[o * (I // gs) + i // gs]) * int(x[t, i])
+                            for i in range(I))
+                assert Fraction(got[t, o]) == exact, (fmt, t, o)
+
+
+# --- step a4: silu and the fused gate/up --------------------------------------
+
+def pin_silu(orc):
+    assert orc.silu(0.0) == 0.0
+    for z in np.linspace(-30, 30, 121):
+        want = z * expit(z)
+        got = orc.silu(float(z))
+        assert abs(got - want) <= 1e-15 * max(1.0, abs(want)), (z, got, want)
+
+
+def pin_gate_up(orc):
+    rng = np.random.default_rng(29)
+    for fmt in ALL_FMTS:
+        F, D, s = 8, 128, 2
+        gs = group_of(fmt, D)
+        cg, cu = random_codes(fmt, F, D, rng), random_codes(fmt, F, D, rng)
+        sg = rng.lognormal(-4, 0.5, size=F * (D // gs)).astype(np.float32)
+        su = rng.lognormal(-4, 0.5, size=F * (D // gs)).astype(np.float32)
+        x = rng.standard_normal((s, D)).astype(np.float32)
+        got = orc.qgate_up(fmt, gs, pack(fmt, cg), sg, pack(fmt, cu), su, x, F, D)
+        g = x.astype(np.float64) @ dense(fmt, cg, sg, gs).T
+        u = x.astype(np.float64) @ dense(fmt, cu, su, gs).T
+        _close(got, g * expit(g) * u)
+        rows = np.array([7, 1])
+        _close(orc.qgate_up_rows(fmt, gs, pack(fmt, cg), sg, pack(fmt, cu), su, x, F, D, rows), got[:, rows])
+
+
+# --- step a5: the routed expert group ----------------------------------------
+
+def _expert_store(fmt, E, D, F, rng):
+    gs_gu, gs_dn = group_of(fmt, D), group_of(fmt, F)
+    cg = [random_codes(fmt, F, D, rng) for _ in range(E)]
+    cu = [random_codes(fmt, F, D, rng) for _ in range(E)]
+    cd = [random_codes(fmt, D, F, rng) for _ in range(E)]
+    sg = [rng.lognormal(-4, 0.5, size=F * (D // gs_gu)).astype(np.float32) for _ in range(E)]
+    su = [rng.lognormal(-4, 0.5, size=F * (D // gs_gu)).astype(np.float32) for _ in range(E)]
+    sd = [rng.lognormal(-4, 0.5, size=D * (F // gs_dn)).astype(np.float32) for _ in range(E)]
+    packed = (np.concatenate([pack(fmt, c) for c in cg]), np.concatenate(sg),
+              np.concatenate([pack(fmt, c) for c in cu]), np.concatenate(su),
+              np.concatenate([pack(fmt, c) for c in cd]), np.concatenate(sd))
+    dense_m = ([dense(fmt, cg[e], sg[e], gs_gu) for e in range(E)],
+               [dense(fmt, cu[e], su[e], gs_gu) for e in range(E)],
+               [dense(fmt, cd[e], sd[e], gs_dn) for e in range(E)])
+    return packed, dense_m
+
+
+def _dense_group(dense_m, x, ids, wts):
+    G, U, Dn = dense_m
+    s, k = ids.shape
+    out = np.zeros((s, Dn[0].shape[0]))
+    for t in range(s):
+        for r in range(k):
+            e = ids[t, r]
+            g = G[e] @ x[t].astype(np.float64)
+            u = U[e] @ x[t].astype(np.float64)
+            out[t] += float(wts[t, r]) * (Dn[e] @ (g * expit(g) * u))
+    return out
+
+
+def pin_expert_group(orc):
+    rng = np.random.default_rng(31)
+    for fmt in ALL_FMTS:
+        E, D, F, s, k = 5, 128, 64, 3, 2
+        gs = group_of(fmt, D) if fmt != INT8_ROW else 0   # int8: one scale per row of each matrix
+        packed, dense_m = _expert_store(fmt, E, D, F, rng)
+        x = rng.standard_normal((s, D)).astype(np.float32)
+        ids = np.array([[0, 3], [4, 4], [2, 1]], dtype=np.int32)   # token 1 routes expert 4 twice
+        wts = rng.random((s, k)).astype(np.float32)
+        got = orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, wts)
+        want = _dense_group(dense_m, x, ids, wts)
+        _close(got, want, rtol=1e-11)
+        # one-hot router weights reduce to one expert's MLP
+        onehot = np.zeros_like(wts)
+        onehot[:, 1] = 1.0
+        _close(orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, onehot),
+               _dense_group(dense_m, x, ids[:, 1:], np.ones((s, 1), np.float32)), rtol=1e-11)
+        # zero router weights give zeros
+        assert not orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, np.zeros_like(wts)).any()
+        # the routed sum does not depend on the order of (id, weight) pairs
+        perm = orc.expert_group(fmt, gs, *packed, E, D, F, x, ids[:, ::-1].copy(), wts[:, ::-1].copy())
+        _close(perm, got, rtol=1e-12)
+        # a sample of output columns equals those columns of the whole output
+        cols = np.array([5, 127, 0])
+        _close(orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, wts, cols=cols), got[:, cols], rtol=1e-14)
+
+
+ALL_PINS = [pin_e2m1, pin_int4_nibbles, pin_int3_planes, pin_int8_bytes, pin_random_codes,
+            pin_dequant_f32, pin_gemv_bruteforce, pin_zero_scales, pin_linearity, pin_integer_exact,
+            pin_silu, pin_gate_up, pin_expert_group]

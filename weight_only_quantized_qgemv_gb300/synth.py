@@ -1,0 +1,209 @@
+"""Seeded synthetic inputs for the quantized GEMV and the routed-expert MLP.
+
+This module only draws random numbers with the distributions of the five
+workloads (uniform codes, lognormal or power-of-two group scales, N(0,1)
+activations, top-k routing with softmax router weights).  It holds none of the
+method's arithmetic: a packed buffer is drawn directly as random bytes, which is
+exactly "uniform codes" for every format because each byte holds whole codes
+(two int4/e2m1 nibbles, four int3 plane-A pairs, eight int3 plane-B bits).
+The GPU path and the CPU oracle both read these buffers; neither lives here.
+
+Layouts drawn (the library's ABI):
+  int8 per row   [O][I] bytes, one f32 scale per row
+  int4 grouped   [O][I/2] bytes (low nibble = even i), f32 scales [O][I/gs]
+  int3-g64       plane A [O][I/4] then plane B [O][I/8] in one buffer,
+                 f32 scales [O][I/64]
+  MXFP4          [O][I/2] bytes of e2m1 nibbles, f32 scales [O][I/32]
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# Format ids as colibri numbers its quantized storages (fmt 1, 4, 5, 7).
+INT8_ROW = 1
+INT4_G = 4
+INT3_G64 = 5
+MXFP4_G32 = 7
+
+FMT_NAMES = {INT8_ROW: "int8_row", INT4_G: "int4_g", INT3_G64: "int3_g64", MXFP4_G32: "mxfp4_g32"}
+
+
+def fixed_group(fmt: int, I: int, gs: int | None = None) -> int:
+    """Group size implied by a format (int8 per row: the whole row)."""
+    if fmt == INT8_ROW:
+        return I
+    if fmt == INT3_G64:
+        return 64
+    if fmt == MXFP4_G32:
+        return 32
+    return 32 if gs is None else gs
+
+
+def packed_bytes(fmt: int, O: int, I: int) -> int:
+    """Bytes of one packed [O][I] matrix."""
+    if fmt == INT8_ROW:
+        return O * I
+    if fmt in (INT4_G, MXFP4_G32):
+        return O * I // 2
+    if fmt == INT3_G64:
+        return O * I // 4 + O * I // 8
+    raise ValueError(f"unknown fmt {fmt}")
+
+
+def generator(seed: int, *spawn_key: int) -> np.random.Generator:
+    """PCG64 stream for (seed, spawn_key...); independent streams per key."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=tuple(spawn_key))))
+
+
+def draw_packed(fmt: int, O: int, I: int, rng: np.random.Generator) -> np.ndarray:
+    """Packed weights with uniform codes (int8: uniform in [-127, 127])."""
+    if fmt == INT8_ROW:
+        return rng.integers(-127, 128, size=O * I, dtype=np.int8).view(np.uint8)
+    return rng.integers(0, 256, size=packed_bytes(fmt, O, I), dtype=np.uint8)
+
+
+def draw_scales(O: int, I: int, gs: int, rng: np.random.Generator, kind: str,
+                mu: float = -4.0, sigma: float = 0.5) -> np.ndarray:
+    """f32 scales [O][I/gs]: 'lognormal' (mu, sigma) or 'pow2' (2^k, k uniform in [-8, 0])."""
+    n = O * (I // gs)
+    if kind == "lognormal":
+        return rng.lognormal(mu, sigma, size=n).astype(np.float32)
+    if kind == "pow2":
+        return np.ldexp(np.ones(n, dtype=np.float32), rng.integers(-8, 1, size=n)).astype(np.float32)
+    raise ValueError(kind)
+
+
+def draw_x(s: int, I: int, rng: np.random.Generator) -> np.ndarray:
+    """Activations x f32 [s][I], N(0, 1)."""
+    return rng.standard_normal(size=(s, I), dtype=np.float32)
+
+
+def draw_routing(s: int, k: int, E: int, rng: np.random.Generator):
+    """Per token: k distinct experts drawn uniformly, router weights = softmax of k N(0,1) logits.
+
+    The router itself runs on the host in the engines the pages describe; here it
+    is replaced by these draws, which the workloads fix.
+    """
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(s)]).astype(np.int32)
+    logits = rng.standard_normal(size=(s, k))
+    w = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    return ids.reshape(s, k), w.reshape(s, k)
+
+
+# ---------------------------------------------------------------------------
+# The five workloads (seed = 1000 + workload index).
+# ---------------------------------------------------------------------------
+
+@dataclass
+class GemvWorkload:
+    name: str
+    fmt: int
+    O: int
+    I: int
+    s: int
+    gs: int
+    scale_kind: str
+    scale_mu: float
+    seed: int
+    x_key: int = 0
+
+    @property
+    def weight_bytes(self) -> int:
+        return packed_bytes(self.fmt, self.O, self.I)
+
+    @property
+    def scale_bytes(self) -> int:
+        return 4 * self.O * (self.I // self.gs)
+
+    def weights(self, copy: int = 0):
+        """(packed uint8, scales f32) for weight copy `copy` (copies differ, same law)."""
+        rng = generator(self.seed, 1, copy)
+        w = draw_packed(self.fmt, self.O, self.I, rng)
+        sc = draw_scales(self.O, self.I, self.gs, rng, self.scale_kind, self.scale_mu)
+        return w, sc
+
+    def x(self):
+        return draw_x(self.s, self.I, generator(self.seed, 2, self.x_key))
+
+
+@dataclass
+class ExpertWorkload:
+    name: str
+    fmt: int
+    E: int
+    D: int
+    F: int
+    s: int
+    k: int
+    gs: int
+    scale_kind: str
+    scale_mu: float
+    seed: int
+    _cache: dict = field(default_factory=dict, repr=False)
+
+    # Matrix ids inside one expert.
+    GATE, UP, DOWN = 0, 1, 2
+
+    def matrix_shape(self, which: int):
+        return (self.F, self.D) if which in (self.GATE, self.UP) else (self.D, self.F)
+
+    def expert_bytes(self) -> int:
+        """Packed + scale bytes of one expert's three matrices."""
+        tot = 0
+        for which in (self.GATE, self.UP, self.DOWN):
+            O, I = self.matrix_shape(which)
+            tot += packed_bytes(self.fmt, O, I) + 4 * O * (I // self.gs)
+        return tot
+
+    def expert_matrix(self, e: int, which: int):
+        """(packed, scales) of expert e's gate/up/down, drawn from its own stream."""
+        O, I = self.matrix_shape(which)
+        rng = generator(self.seed, 10, e, which)
+        w = draw_packed(self.fmt, O, I, rng)
+        sc = draw_scales(O, I, self.gs, rng, self.scale_kind, self.scale_mu)
+        return w, sc
+
+    def x(self, step: int = 0):
+        return draw_x(self.s, self.D, generator(self.seed, 2, step))
+
+    def routing(self, step: int = 0):
+        return draw_routing(self.s, self.k, self.E, generator(self.seed, 3, step))
+
+
+def workload(name: str):
+    """The named workload.  Names state format, sizes and batch."""
+    table = {
+        # int8 per row, 1024 x 1024, s = 1; row scales lognormal(-5, 0.5).
+        "int8_row_1024x1024_s1": GemvWorkload("int8_row_1024x1024_s1", INT8_ROW, 1024, 1024, 1, 1024,
+                                               "lognormal", -5.0, 1001),
+        # int4 group 32, O = 16384, I = 6144, s = 1 and s = 4; scales lognormal(-4, 0.5).
+        "int4_g32_16384x6144_s1": GemvWorkload("int4_g32_16384x6144_s1", INT4_G, 16384, 6144, 1, 32,
+                                                "lognormal", -4.0, 1002),
+        "int4_g32_16384x6144_s4": GemvWorkload("int4_g32_16384x6144_s4", INT4_G, 16384, 6144, 4, 32,
+                                                "lognormal", -4.0, 1002, x_key=4),
+        # int3-g64 dual plane, O = 6144, I = 16384 (o_proj-like long rows), s = 1.
+        "int3_g64_6144x16384_s1": GemvWorkload("int3_g64_6144x16384_s1", INT3_G64, 6144, 16384, 1, 64,
+                                                "lognormal", -4.0, 1003),
+        # MXFP4 expert MLP, one token, top-8 of 256 experts; scales 2^k, k in [-8, 0].
+        "mxfp4_experts_E256_D6144_F2048_s1_k8": ExpertWorkload("mxfp4_experts_E256_D6144_F2048_s1_k8",
+                                                               MXFP4_G32, 256, 6144, 2048, 1, 8, 32,
+                                                               "pow2", 0.0, 1004),
+        # int4-g32 expert group, 8 tokens, top-8 of 256 experts each.
+        "int4_g32_experts_E256_D6144_F2048_s8_k8": ExpertWorkload("int4_g32_experts_E256_D6144_F2048_s8_k8",
+                                                                  INT4_G, 256, 6144, 2048, 8, 8, 32,
+                                                                  "lognormal", -4.0, 1005),
+    }
+    return table[name]
+
+
+WORKLOADS = [
+    "int8_row_1024x1024_s1",
+    "int4_g32_16384x6144_s1",
+    "int4_g32_16384x6144_s4",
+    "int3_g64_6144x16384_s1",
+    "mxfp4_experts_E256_D6144_F2048_s1_k8",
+    "int4_g32_experts_E256_D6144_F2048_s8_k8",
+]
