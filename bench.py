@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""Throughput bench of the quantized GEMV / routed-expert library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints ONE JSON line (rank 0).  A step is one call of the hot path on one
+batch of synthetic input of the named workload (default: the int4 group-32
+GEMV, O = 16384, I = 6144, s = 1).  `value` is weight + scale bytes streamed
+per second over the whole job (all ranks); the device timing replays a CUDA
+graph of back-to-back calls with inputs resident in HBM, rotating over weight
+copies that together exceed twice the L2 (or over fresh routings of the 6 GB
+expert store), so no call finds its weights in L2.  `e2e` is the same metric
+through the public API with pinned host buffers: each step copies its inputs
+host->device and reads its result back.  With more than one rank (torchrun)
+every rank runs an independent replica: the path has no exchange step.
+
+--impl reference times the plain f64 CPU oracle on host cores, on bounded
+samples of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from weight_only_quantized_qgemv_gb300 import synth  # noqa: E402
+
+METRIC = "achieved weight-stream GB/s (% of GB300 HBM peak); µs per fused expert group"
+DEFAULT_WORKLOAD = "int4_g32_16384x6144_s1"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+FMT_LABEL = {1: "int8-row", 4: "int4-g", 5: "int3-g64", 7: "mxfp4-g32"}
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, traffic record
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qgemv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [c.strip() for c in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+                power.append(float(p[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.remove(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "weight_only_quantized_qgemv_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary for this workload, if it was taken on the current sources."""
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path).read()
+        if f"workload: {workload}\n" not in text:
+            continue
+        m = re.search(r"traffic_bytes_per_launch: (\d+)", text)
+        hm = re.search(r"source_hash: (\w+)", text)
+        if m and hm and hm.group(1) == source_hash():
+            return int(m.group(1))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# workloads on the device
+# ---------------------------------------------------------------------------
+class GemvBench:
+    def __init__(self, wl, device, l2_bytes):
+        import torch
+        self.wl = wl
+        self.torch = torch
+        self.step_bytes = wl.weight_bytes + wl.scale_bytes
+        self.ncopies = max(2, -(-2 * l2_bytes // self.step_bytes) + 1)
+        self.w, self.sc = [], []
+        for c in range(self.ncopies):
+            w, sc = wl.weights(copy=c)
+            self.w.append(torch.from_numpy(w).to(device))
+            self.sc.append(torch.from_numpy(sc).to(device))
+        self.x_host = wl.x()
+        self.x = torch.from_numpy(self.x_host).to(device)
+        self.y = torch.empty(wl.s, wl.O, dtype=torch.float32, device=device)
+        self.gs = wl.gs if wl.fmt == synth.INT4_G else 0
+        self.launches_per_step = 1
+        self.l2_note = f"rotates {self.ncopies} weight copies ({self.ncopies * self.step_bytes / 1e6:.0f} MB > 2x L2)"
+
+    def step(self, i, stream):
+        from weight_only_quantized_qgemv_gb300 import qgemv
+        c = i % self.ncopies
+        wl = self.wl
+        qgemv(wl.fmt, self.gs, self.w[c], self.sc[c], self.x, wl.O, wl.I, wl.s, self.y, stream)
+
+    def bytes_of(self, i):
+        return self.step_bytes
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.x_pin = torch.from_numpy(self.x_host.copy()).pin_memory()
+        self.y_pin = torch.empty(self.wl.s, self.wl.O, dtype=torch.float32).pin_memory()
+        return self.x_pin.numel() * 4, self.y_pin.numel() * 4
+
+    def e2e_step(self, i, stream):
+        from weight_only_quantized_qgemv_gb300 import qgemv
+        wl = self.wl
+        c = i % self.ncopies
+        self.x.copy_(self.x_pin, non_blocking=True)
+        qgemv(wl.fmt, self.gs, self.w[c], self.sc[c], self.x, wl.O, wl.I, wl.s, self.y, stream)
+        self.y_pin.copy_(self.y, non_blocking=True)
+
+    def config(self):
+        cfg = gemv_config(self.wl)
+        cfg["l2"] = self.l2_note
+        return cfg
+
+
+class ExpertBench:
+    def __init__(self, wl, device, nsteps):
+        import torch
+        from weight_only_quantized_qgemv_gb300 import qexpert_group_workspace
+        self.wl = wl
+        self.torch = torch
+        self.d = {}
+        for name, which in wl.MATRICES:
+            nb, ns = wl.sizes(which)
+            self.d[name] = torch.empty(wl.E * nb, dtype=torch.uint8, device=device)
+            self.d[name + "_s"] = torch.empty(wl.E * ns, dtype=torch.float32, device=device)
+
+        def sink(name, slot, w, sc):
+            self.d[name][slot * w.size:(slot + 1) * w.size].copy_(torch.from_numpy(w))
+            self.d[name + "_s"][slot * sc.size:(slot + 1) * sc.size].copy_(torch.from_numpy(sc))
+
+        wl.generate(range(wl.E), sink)
+        torch.cuda.synchronize()
+        self.nroutes = max(64, min(nsteps, 4096))
+        ids, wts, xs = [], [], []
+        for r in range(self.nroutes):
+            i, w = wl.routing(step=r)
+            ids.append(i)
+            wts.append(w)
+            xs.append(wl.x(step=r))
+        self.ids_host = np.stack(ids).astype(np.int32)
+        self.wts_host = np.stack(wts).astype(np.float32)
+        self.x_host = np.stack(xs).astype(np.float32)
+        self.ids = torch.from_numpy(self.ids_host).to(device)
+        self.wts = torch.from_numpy(self.wts_host).to(device)
+        self.x = torch.from_numpy(self.x_host).to(device)
+        self.out = torch.empty(wl.s, wl.D, dtype=torch.float32, device=device)
+        self.ws_bytes = qexpert_group_workspace(wl.E, wl.D, wl.F, wl.s, wl.k)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.gs = wl.gs if wl.fmt == synth.INT4_G else 0
+        self.expert_bytes = wl.expert_bytes()
+        self.route_bytes = [len(np.unique(self.ids_host[r])) * self.expert_bytes for r in range(self.nroutes)]
+        self.launches_per_step = 4
+
+    def _call(self, r, x, ids, wts, stream):
+        from weight_only_quantized_qgemv_gb300 import qexpert_group
+        wl, d = self.wl, self.d
+        qexpert_group(wl.fmt, self.gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"],
+                      wl.E, wl.D, wl.F, x, wl.s, wl.k, ids, wts, self.out, self.ws, self.ws_bytes,
+                      self.status, stream)
+
+    def step(self, i, stream):
+        r = i % self.nroutes
+        self._call(r, self.x[r], self.ids[r], self.wts[r], stream)
+
+    def bytes_of(self, i):
+        return self.route_bytes[i % self.nroutes]
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.x_pin = torch.from_numpy(self.x_host.copy()).pin_memory()
+        self.ids_pin = torch.from_numpy(self.ids_host.copy()).pin_memory()
+        self.wts_pin = torch.from_numpy(self.wts_host.copy()).pin_memory()
+        self.out_pin = torch.empty(self.wl.s, self.wl.D, dtype=torch.float32).pin_memory()
+        self.x1 = torch.empty_like(self.x[0])
+        self.ids1 = torch.empty_like(self.ids[0])
+        self.wts1 = torch.empty_like(self.wts[0])
+        h2d = (self.x1.numel() + self.ids1.numel() + self.wts1.numel()) * 4
+        return h2d, self.out_pin.numel() * 4
+
+    def e2e_step(self, i, stream):
+        r = i % self.nroutes
+        self.x1.copy_(self.x_pin[r], non_blocking=True)
+        self.ids1.copy_(self.ids_pin[r], non_blocking=True)
+        self.wts1.copy_(self.wts_pin[r], non_blocking=True)
+        self._call(r, self.x1, self.ids1, self.wts1, stream)
+        self.out_pin.copy_(self.out, non_blocking=True)
+
+    def config(self):
+        wl = self.wl
+        cfg = expert_config(wl)
+        cfg["l2"] = f"{self.nroutes} seeded routings over the {wl.E * self.expert_bytes / 1e9:.2f} GB store (> L2)"
+        cfg["mean_experts_per_step"] = float(np.mean([len(np.unique(r)) for r in self.ids_host]))
+        return cfg
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ---------------------------------------------------------------------------
+def oracle_sample_runner(wl, target_s: float):
+    """A callable running the oracle on a sample of the workload, the bytes it
+    covers, and a description.  Sized to ~target_s seconds."""
+    from oracle import oracle as orc
+
+    if isinstance(wl, synth.GemvWorkload):
+        w, sc = wl.weights()
+        x = wl.x()
+        per_row = (wl.weight_bytes + wl.scale_bytes) // wl.O
+
+        def run(nrows, start=0):
+            rows = (np.arange(nrows) + start) % wl.O
+            orc.qgemv_rows(wl.fmt, wl.gs, w, sc, x, wl.O, wl.I, rows)
+            return nrows * per_row
+
+        t = time.perf_counter()
+        run(16)
+        dt = max(time.perf_counter() - t, 1e-6) / 16
+        nrows = int(max(16, min(wl.O, target_s / dt)))
+        return (lambda i=0: run(nrows, start=i * nrows)), f"{nrows} of {wl.O} rows, all {wl.s} activation rows"
+
+    # expert group: gate/up rows of the first routed expert of token 0 (the
+    # oracle's fused gate/up arithmetic), sized to the target time
+    ids, _ = wl.routing(step=0)
+    x = wl.x(step=0)[:1]
+    st = wl.store(ids[0, :1])
+    per_row = 2 * (synth.packed_bytes(wl.fmt, 1, wl.D) + 4 * (wl.D // wl.gs))
+
+    def run_rows(nrows, start=0):
+        rows = (np.arange(nrows) + start) % wl.F
+        orc.qgate_up_rows(wl.fmt, wl.gs, st["gate"], st["gate_s"], st["up"], st["up_s"], x, wl.F, wl.D, rows)
+        return nrows * per_row
+
+    t = time.perf_counter()
+    run_rows(16)
+    dt = max(time.perf_counter() - t, 1e-6) / 16
+    nrows = int(max(16, min(wl.F, target_s / dt)))
+    return ((lambda i=0: run_rows(nrows, start=i * nrows)),
+            f"{nrows} of {wl.F} gate/up rows of expert {int(ids[0, 0])} (token 0, first routing)")
+
+
+def cpu_baseline(wl, target_s=12.0):
+    from oracle import oracle as orc
+    run, desc = oracle_sample_runner(wl, target_s)
+    t = time.perf_counter()
+    nbytes = run()
+    dt = time.perf_counter() - t
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": orc.threads(), "kind": "oracle",
+            "sample": desc + f"; {dt:.1f} s"}
+
+
+def reference_arm(args, wl, world, rank):
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    orc.build()
+    run, desc = oracle_sample_runner(wl, target_s=max(0.5, 60.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        run(i)
+    t = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        nbytes += run(args.warmup + i)
+    dt = time.perf_counter() - t
+    value = nbytes / dt / 1e9
+    cfg = gemv_config(wl) if isinstance(wl, synth.GemvWorkload) else expert_config(wl)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": orc.threads(), "kind": "oracle",
+                             "sample": desc + " per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def gemv_config(wl):
+    return {"workload": wl.name, "kind": "qgemv", "fmt": FMT_LABEL[wl.fmt] + (str(wl.gs) if wl.fmt == 4 else ""),
+            "O": wl.O, "I": wl.I, "s": wl.s, "gs": wl.gs, "parallelism": "replicas"}
+
+
+def expert_config(wl):
+    return {"workload": wl.name, "kind": "qexpert_group", "fmt": FMT_LABEL[wl.fmt] + (str(wl.gs) if wl.fmt == 4 else ""),
+            "E": wl.E, "D": wl.D, "F": wl.F, "s": wl.s, "k": wl.k, "gs": wl.gs, "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-len", type=int, default=64, help="calls captured per CUDA graph replay")
+    args = ap.parse_args()
+    wl = synth.workload(args.workload)
+    world, rank, local = dist_env()
+    if args.steps is None:
+        # about one second of timed device work, so the clock samples mean something
+        if isinstance(wl, synth.GemvWorkload):
+            est = (wl.weight_bytes + wl.scale_bytes) / 6e12 + 3e-6
+        else:
+            est = 0.9 * wl.s * wl.k * wl.expert_bytes() / 6e12 + 12e-6
+        args.steps = int(min(200000, max(1000, 1.0 / est)))
+    args.warmup = max(3, args.warmup)
+
+    if args.impl == "reference":
+        reference_arm(args, wl, world, rank)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from weight_only_quantized_qgemv_gb300 import _build, _lib
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    barrier(world)
+    _lib.lib()
+
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024
+    bench = GemvBench(wl, device, l2) if isinstance(wl, synth.GemvWorkload) else ExpertBench(wl, device, args.steps)
+    stream = torch.cuda.Stream(device)
+
+    # warm-up: eager steps, then build the graph (its capture also warms up)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            bench.step(i, stream.cuda_stream)
+    stream.synchronize()
+    G = max(1, min(args.graph_len, args.steps))
+    graphs = []
+    period = bench.ncopies if isinstance(bench, GemvBench) else bench.nroutes
+    ngraphs = max(1, min(-(-period // G), -(-args.steps // G)))
+    for gi in range(ngraphs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(G):
+                bench.step(gi * G + j, torch.cuda.current_stream().cuda_stream)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+    stream.synchronize()
+
+    reps = -(-args.steps // G)
+    steps_done = reps * G
+    nbytes = sum(bench.bytes_of(((r % ngraphs) * G) + j) for r in range(reps) for j in range(G))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for r in range(reps):
+                graphs[r % ngraphs].replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    t_dev = ev0.elapsed_time(ev1) / 1e3
+    clocks = clk.summary()
+    t_max = reduce_max(t_dev, world, device)
+    total_bytes = reduce_sum(float(nbytes), world, device)
+    value = total_bytes / t_max / 1e9
+    per_launch_s = t_dev / steps_done
+    achieved = (nbytes / steps_done) / per_launch_s / 1e9
+    peak, peak_src = hbm_peak()
+
+    # end to end through the public API, host buffers, copies inside the timed region
+    h2d, d2h = bench.e2e_setup()
+    k_e2e = min(args.steps, 2000)
+    barrier(world)
+    torch.cuda.synchronize()
+    e2e_bytes = 0
+    t = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(k_e2e):
+            bench.e2e_step(i, stream.cuda_stream)
+            stream.synchronize()
+            e2e_bytes += bench.bytes_of(i)
+    t_e2e = reduce_max(time.perf_counter() - t, world, device)
+    e2e_value = reduce_sum(float(e2e_bytes), world, device) / t_e2e / 1e9
+    barrier(world)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+    cfg = bench.config()
+    cfg["graph_calls_per_replay"] = G
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps_done,
+        "warmup": args.warmup, "ms_per_step": t_max / steps_done * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+        "us_per_call": per_launch_s * 1e6,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_src}",
+                     "frac_of_8000": achieved / NOMINAL_HBM_GBS,
+                     "traffic": recorded_traffic(wl.name),
+                     "algorithmic_bytes_per_launch": nbytes / steps_done,
+                     "kernel": "k_stream (qgemv)" if isinstance(bench, GemvBench)
+                     else "qexpert_group call (prep + gate/up + down + combine)"},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": k_e2e, "us_per_step": t_e2e / k_e2e * 1e6},
+        "gpu_launches": steps_done * bench.launches_per_step,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * qgemv.h -- C ABI of the GB300 (sm_103a) weight-only quantized GEMV library.
+ *
+ * The operations are the decode-time primitives of colibri's GPU backends:
+ *   qgemv          one quantized GEMV                 ("colibri Vulkan 计算后端完全指南",
+ *                                                      xdnf.cn, section "API 契约":
+ *                                                      coli_vk_matmul)
+ *   qgate_up       silu(gate x) * (up x), x read once (same section: coli_vk_gate_up)
+ *   qexpert_group  the fused gate/up -> down MLP of a batch of routed experts,
+ *                  summed with router weights in routing order
+ *                                                     (same section:
+ *                                                      coli_vk_expert_group; colibri
+ *                                                      docs/vulkan.md, the expert tier:
+ *                                                      "every expert's output joins
+ *                                                      its row in routing (rank) order")
+ *   qdequant       the dequantized weights as f32, for checking the decoders
+ * The formats are those of the same guide's section "着色器层面的实现细节":
+ * int8, int4 decoded nibble - 8 with one f32 scale per group, int3-g64 in two
+ * bit planes with one f32 scale per 64 inputs, and MXFP4 (e2m1 nibbles, bit 3
+ * the sign) whose scale the host has expanded to f32 per 32 inputs.
+ *
+ * Conventions for every call:
+ *  - All array pointers are DEVICE pointers, owned by the caller.  The library
+ *    allocates no device memory and keeps no state between calls; scratch
+ *    that a call needs (qexpert_group) is a caller-provided workspace.
+ *  - Calls are asynchronous on the given CUDA stream (`stream` is a
+ *    cudaStream_t; NULL is the legacy default stream).  They return once the
+ *    work is enqueued; the caller synchronizes before reading results.
+ *  - Every call returns a status: QSTATUS_OK (0) or a negative code.  On a
+ *    negative return nothing was enqueued, except QSTATUS_LAUNCH (a CUDA error
+ *    at launch; qlast_cuda_error() has its text).  There is no CPU fallback.
+ *  - Matrices are row-major, O rows of I inputs.  Element (o, i) takes the scale
+ *    scales[o * (I / gs) + i / gs] (groups run along a row).  Packed layouts:
+ *      QFMT_INT8_ROW   int8 codes [O][I], value = code; one scale per row
+ *                      (gs must be 0 or I).
+ *      QFMT_INT4_G     [O][I/2] bytes, the low nibble holds the even input i,
+ *                      value = nibble - 8; gs a power of two >= 32.
+ *      QFMT_INT3_G64   plane A [O][I/4] (the low two bits of four codes per
+ *                      byte, least significant first) followed in the same
+ *                      buffer by plane B [O][I/8] (the high bit of eight codes
+ *                      per byte); value = code - 4; gs must be 0 or 64.
+ *      QFMT_MXFP4_G32  [O][I/2] bytes of e2m1 nibbles, the low nibble holds the
+ *                      even input; gs must be 0 or 32.
+ *  - Alignment: packed weights and activation/hidden vectors (x, h, workspace)
+ *    16-byte aligned; scales and outputs 4-byte aligned; else QSTATUS_MISALIGNED.
+ *  - Sizes: I % 16 == 0 (int8), I % gs == 0 (grouped formats), O, I, s >= 1;
+ *    the activation rows of one launch are staged in shared memory, so
+ *    I <= 51200 (else QSTATUS_BAD_DIM).
+ */
+#ifndef QGEMV_GB300_H
+#define QGEMV_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight formats (colibri's storage ids). */
+enum {
+    QFMT_INT8_ROW = 1,
+    QFMT_INT4_G = 4,
+    QFMT_INT3_G64 = 5,
+    QFMT_MXFP4_G32 = 7
+};
+
+/* Status codes. */
+enum {
+    QSTATUS_OK = 0,
+    QSTATUS_BAD_FMT = -1,        /* unknown format id, or gs not allowed for it */
+    QSTATUS_BAD_DIM = -2,        /* a size out of range or not a multiple it must be */
+    QSTATUS_MISALIGNED = -3,     /* a pointer without the alignment stated above */
+    QSTATUS_NULL = -4,           /* a required pointer is NULL */
+    QSTATUS_WORKSPACE = -5,      /* workspace smaller than qexpert_group_workspace() */
+    QSTATUS_LAUNCH = -6,         /* CUDA reported an error at launch */
+    QSTATUS_DEVICE_TIMEOUT = -7, /* a bounded device-side wait ran out */
+    QSTATUS_BAD_EXPERT_ID = -8   /* an expert id outside [0, E) (reported on the device) */
+};
+
+/*
+ * y[t][o] = sum_i value(W[o][i]) * scales[o][i/gs] * x[t][i],  t < s, o < O.
+ *   w       packed weights (layout above)
+ *   scales  f32 [O][I/gs]
+ *   x       f32 [s][I]
+ *   y       f32 [s][O], written
+ * Weights are streamed once per group of up to 8 activation rows; larger s is
+ * processed in groups of 8.
+ */
+int qgemv(int fmt, int gs, const void* w, const float* scales,
+          const float* x, int O, int I, int s, float* y, void* stream);
+
+/*
+ * h[t][f] = silu(g) * u with g = gate[f] . x[t], u = up[f] . x[t], and
+ * silu(z) = z / (1 + e^-z); gate and up are F x D matrices of one format.
+ *   x  f32 [s][D];  h  f32 [s][F], written.
+ */
+int qgate_up(int fmt, int gs, const void* wg, const float* sg,
+             const void* wu, const float* su,
+             const float* x, int F, int D, int s, float* h, void* stream);
+
+/* Bytes of workspace qexpert_group needs for these sizes. */
+size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
+
+/*
+ * The routed-expert MLP of s tokens, each routed to k experts:
+ *   out[t] = sum_{r=0}^{k-1} w[t][r] * down_e (silu(gate_e x_t) * (up_e x_t)),
+ *   e = ids[t][r], summed in rank order r for every t.
+ *   gate, up  packed [E][F][D] (expert e's F x D matrix at e * its size),
+ *             scales f32 [E][F][D/gs]
+ *   down      packed [E][D][F], scales f32 [E][D][F/gs]   (int8: one per row)
+ *   x         f32 [s][D];  ids int32 [s][k];  wts f32 [s][k]
+ *   out       f32 [s][D], written
+ *   workspace device scratch of ws_bytes >= qexpert_group_workspace(E, D, F, s, k)
+ *             bytes; its contents on entry do not matter.
+ *   status_dev optional device int32: set to QSTATUS_OK, or to
+ *             QSTATUS_BAD_EXPERT_ID when an id is outside [0, E) -- then out is
+ *             all zeros.  The host-side return cannot see device-side checks.
+ * Each expert's weights are streamed once for all the (token, rank) pairs
+ * routed to it; repeated ids in a row are allowed and summed.  s * k <= 4096.
+ */
+int qexpert_group(int fmt, int gs,
+                  const void* gate, const float* gate_s,
+                  const void* up, const float* up_s,
+                  const void* down, const float* down_s,
+                  int E, int D, int F,
+                  const float* x, int s, int k,
+                  const int32_t* ids, const float* wts,
+                  float* out, void* workspace, size_t ws_bytes,
+                  int32_t* status_dev, void* stream);
+
+/*
+ * out[o][i] = value(W[o][i]) * scales[o][i/gs] as f32 (one IEEE f32
+ * multiplication of the exact code value by the scale).  For checking the
+ * decoders bit for bit; out f32 [O][I].
+ */
+int qdequant(int fmt, int gs, const void* w, const float* scales,
+             int O, int I, float* out, void* stream);
+
+/* A static description of a status code. */
+const char* qstatus_string(int status);
+
+/* Text of the CUDA error behind the calling thread's last QSTATUS_LAUNCH. */
+const char* qlast_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_GB300_H */

@@ -1,0 +1,100 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from weight_only_quantized_qgemv_gb300 import _build, _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()          # nvcc cross-compiles sm_103a without a GPU
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(q\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["qgemv", "qgate_up", "qexpert_group", "qexpert_group_workspace", "qdequant", "qstatus_string",
+              "qlast_cuda_error"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/qgemv.h but not exported"
+        ctypes.cast(getattr(L, name), ctypes.c_void_p)
+
+
+def test_status_strings(L):
+    for st in range(0, -9, -1):
+        assert _lib.qstatus_string(st)
+    assert "unknown" in _lib.qstatus_string(-100)
+
+
+# Fake but 256-byte aligned device addresses: the checks below fail before any
+# pointer is used.
+A = 1 << 20
+
+
+@pytest.mark.parametrize("fmt,gs,I,want", [
+    (2, 32, 1024, -1),          # unknown format
+    (4, 48, 1024, -1),          # int4 group size not a power of two
+    (4, 16, 1024, -1),          # int4 group below 32
+    (5, 32, 1024, -1),          # int3 is group 64 only
+    (7, 64, 1024, -1),          # MXFP4 is group 32 only
+    (1, 32, 1024, -1),          # int8 per row: gs must be 0 or I
+    (1, 0, 1000, -2),           # int8 row not a multiple of 16
+    (4, 64, 1056, -2),          # I not a multiple of gs
+    (5, 0, 1000, -2),           # int3 I not a multiple of 64
+    (4, 32, 51232, -2),         # row longer than the staging limit
+])
+def test_qgemv_rejects_bad_formats_and_sizes(L, fmt, gs, I, want):
+    assert L.qgemv(fmt, gs, A, A, A, 16, I, 1, A, None) == want
+
+
+def test_qgemv_rejects_null_and_misaligned(L):
+    assert L.qgemv(4, 32, None, A, A, 16, 1024, 1, A, None) == -4
+    assert L.qgemv(4, 32, A, A, None, 16, 1024, 1, A, None) == -4
+    assert L.qgemv(4, 32, A + 8, A, A, 16, 1024, 1, A, None) == -3     # weights need 16 B
+    assert L.qgemv(4, 32, A, A, A + 4, 16, 1024, 1, A, None) == -3     # x needs 16 B
+    assert L.qgemv(4, 32, A, A + 2, A, 16, 1024, 1, A, None) == -3     # scales need 4 B
+    assert L.qgemv(4, 32, A, A, A, 0, 1024, 1, A, None) == -2          # O >= 1
+    assert L.qgemv(4, 32, A, A, A, 16, 1024, 0, A, None) == -2         # s >= 1
+
+
+def test_qgate_up_and_dequant_checks(L):
+    assert L.qgate_up(4, 32, A, A, A, A, A, 16, 1000, 1, A, None) == -2
+    assert L.qgate_up(4, 32, A, A, None, A, A, 16, 1024, 1, A, None) == -4
+    assert L.qdequant(9, 32, A, A, 16, 1024, A, None) == -1
+    assert L.qdequant(4, 32, A, A, 16, 1024, None, None) == -4
+
+
+def test_expert_group_checks(L):
+    ws = _lib.qexpert_group_workspace(256, 6144, 2048, 8, 8)
+    assert ws >= 64 * (6144 + 2048) * 4
+    args = [4, 32, A, A, A, A, A, A, 256, 6144, 2048, A, 8, 8, A, A, A, A, ws, None, None]
+    bad = list(args)
+    bad[18] = ws - 1
+    assert L.qexpert_group(*bad) == -5                 # workspace too small
+    bad = list(args)
+    bad[17] = A + 16
+    assert L.qexpert_group(*bad) == -3                 # workspace must be 256-byte aligned
+    bad = list(args)
+    bad[12], bad[13] = 1024, 8                         # s * k above 4096
+    assert L.qexpert_group(*bad) == -2
+    bad = list(args)
+    bad[10] = 2050                                     # F not a multiple of the group
+    assert L.qexpert_group(*bad) == -2
+    assert _lib.qexpert_group_workspace(0, 6144, 2048, 8, 8) >= 0

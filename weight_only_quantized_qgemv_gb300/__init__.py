@@ -1,0 +1,10 @@
+"""Weight-only group-quantized GEMV and routed-expert MLP for GB300 (sm_103a).
+
+The computation lives in a CUDA shared library with a C ABI (include/qgemv.h);
+this package holds its sources (csrc/), the build step, a thin ctypes binding
+with the same entry-point names, and the seeded synthetic workloads.
+"""
+from ._lib import (QFMT_INT3_G64, QFMT_INT4_G, QFMT_INT8_ROW, QFMT_MXFP4_G32, QStatusError,  # noqa: F401
+                   library_path, qdequant, qexpert_group, qexpert_group_workspace, qgate_up, qgemv,
+                   qstatus_string)
+from ._build import build  # noqa: F401

@@ -1,0 +1,123 @@
+"""Thin ctypes binding of the C ABI in include/qgemv.h.
+
+Argument marshalling only: every computation runs in the CUDA library.  Array
+arguments may be torch tensors (their data_ptr() is passed) or raw integer
+device addresses; `stream` defaults to torch's current CUDA stream.  A negative
+status raises QStatusError.  If the library has not been built, loading fails
+loudly -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+QFMT_INT8_ROW, QFMT_INT4_G, QFMT_INT3_G64, QFMT_MXFP4_G32 = 1, 4, 5, 7
+
+QSTATUS = {
+    0: "QSTATUS_OK",
+    -1: "QSTATUS_BAD_FMT",
+    -2: "QSTATUS_BAD_DIM",
+    -3: "QSTATUS_MISALIGNED",
+    -4: "QSTATUS_NULL",
+    -5: "QSTATUS_WORKSPACE",
+    -6: "QSTATUS_LAUNCH",
+    -7: "QSTATUS_DEVICE_TIMEOUT",
+    -8: "QSTATUS_BAD_EXPERT_ID",
+}
+
+
+class QStatusError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{QSTATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"the CUDA library {path} is not built; run __graft_entry__.build() "
+                               "(nvcc, sm_103a) first -- there is no CPU fallback")
+        L = ctypes.CDLL(path)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.qgemv.argtypes = [I, I, P, P, P, I, I, I, P, P]
+        L.qgemv.restype = I
+        L.qgate_up.argtypes = [I, I, P, P, P, P, P, I, I, I, P, P]
+        L.qgate_up.restype = I
+        L.qexpert_group_workspace.argtypes = [I, I, I, I, I]
+        L.qexpert_group_workspace.restype = Z
+        L.qexpert_group.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, P, P, P, P, Z, P, P]
+        L.qexpert_group.restype = I
+        L.qdequant.argtypes = [I, I, P, P, I, I, P, P]
+        L.qdequant.restype = I
+        L.qstatus_string.argtypes = [I]
+        L.qstatus_string.restype = ctypes.c_char_p
+        L.qlast_cuda_error.argtypes = []
+        L.qlast_cuda_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != 0:
+        L = lib()
+        msg = L.qstatus_string(status).decode()
+        if status == -6:
+            msg += f" ({L.qlast_cuda_error().decode()})"
+        raise QStatusError(status, msg)
+
+
+def qstatus_string(status: int) -> str:
+    return lib().qstatus_string(status).decode()
+
+
+def qgemv(fmt, gs, w, scales, x, O, I, s, y, stream=None):
+    _check(lib().qgemv(fmt, gs, _ptr(w), _ptr(scales), _ptr(x), O, I, s, _ptr(y), _stream(stream)))
+
+
+def qgate_up(fmt, gs, wg, sg, wu, su, x, F, D, s, h, stream=None):
+    _check(lib().qgate_up(fmt, gs, _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(x), F, D, s, _ptr(h),
+                          _stream(stream)))
+
+
+def qexpert_group_workspace(E, D, F, s, k) -> int:
+    return lib().qexpert_group_workspace(E, D, F, s, k)
+
+
+def qexpert_group(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, out,
+                  workspace, ws_bytes, status_dev=None, stream=None):
+    _check(lib().qexpert_group(fmt, gs, _ptr(gate), _ptr(gate_s), _ptr(up), _ptr(up_s), _ptr(down),
+                               _ptr(down_s), E, D, F, _ptr(x), s, k, _ptr(ids), _ptr(wts), _ptr(out),
+                               _ptr(workspace), ws_bytes, _ptr(status_dev), _stream(stream)))
+
+
+def qdequant(fmt, gs, w, scales, O, I, out, stream=None):
+    _check(lib().qdequant(fmt, gs, _ptr(w), _ptr(scales), O, I, _ptr(out), _stream(stream)))

@@ -1,0 +1,330 @@
+// qg_abi.cu -- the C entry points: argument checks, launch set-up, and the
+// format-independent kernels of the routed-expert group (grouping the
+// (token, rank) pairs by expert, and the rank-order weighted sum).
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "qg_internal.h"
+
+namespace qg {
+
+static thread_local const char* g_last_cuda_error = "no error";
+
+static int launch_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return QSTATUS_OK;
+    g_last_cuda_error = cudaGetErrorString(e);
+    return QSTATUS_LAUNCH;
+}
+
+// Number of SMs of the current device (read once per device).
+static int sm_count(int* status)
+{
+    static int cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { *status = launch_status(e); return 0; }
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || n <= 0) { *status = launch_status(e == cudaSuccess ? cudaErrorInvalidDevice : e); return 0; }
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Resolves and checks the group size of an O x I matrix in format fmt.
+static int check_fmt(int fmt, int gs, int I, int* gs_out)
+{
+    switch (fmt) {
+    case QFMT_INT8_ROW:
+        if (gs != 0 && gs != I) return QSTATUS_BAD_FMT;
+        if (I % 16) return QSTATUS_BAD_DIM;
+        *gs_out = I;
+        return QSTATUS_OK;
+    case QFMT_INT4_G:
+        if (gs < 32 || (gs & (gs - 1))) return QSTATUS_BAD_FMT;
+        if (I % gs) return QSTATUS_BAD_DIM;
+        *gs_out = gs;
+        return QSTATUS_OK;
+    case QFMT_INT3_G64:
+        if (gs != 0 && gs != 64) return QSTATUS_BAD_FMT;
+        if (I % 64) return QSTATUS_BAD_DIM;
+        *gs_out = 64;
+        return QSTATUS_OK;
+    case QFMT_MXFP4_G32:
+        if (gs != 0 && gs != 32) return QSTATUS_BAD_FMT;
+        if (I % 32) return QSTATUS_BAD_DIM;
+        *gs_out = 32;
+        return QSTATUS_OK;
+    default:
+        return QSTATUS_BAD_FMT;
+    }
+}
+
+constexpr int kMaxI = 51200;   // one activation row of I f32 must fit the staging buffer
+
+static int rows_per_launch(int I)
+{
+    int s = kSmemMax / (I * (int)sizeof(float));
+    return s < kSmax ? s : kSmax;
+}
+
+#define QG_FMT_SWITCH(fmt, CALL)                                 \
+    switch (fmt) {                                               \
+    case QFMT_INT8_ROW: e = CALL(int8); break;                   \
+    case QFMT_INT4_G: e = CALL(int4); break;                     \
+    case QFMT_INT3_G64: e = CALL(int3); break;                   \
+    default: e = CALL(mxfp4); break;                             \
+    }
+
+// ---------------------------------------------------------------------------
+// Expert group: (token, rank) pairs sorted by (expert, pair index), split into
+// batches of at most smax pairs of one expert.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_expert_prep(const int32_t* __restrict__ ids, int P, int k, int E, int smax,
+                                                      unsigned char* ws, WsLayout L, int32_t* status_dev)
+{
+    __shared__ int s_ids[kMaxPairs];
+    __shared__ int s_sorted[kMaxPairs];
+    __shared__ int s_bad;
+    int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+    int4* batches = reinterpret_cast<int4*>(ws + L.batches);
+    int32_t* pair_tok = reinterpret_cast<int32_t*>(ws + L.pair_tok);
+    int32_t* pair_of = reinterpret_cast<int32_t*>(ws + L.pair_of);
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = ids[p];
+        s_ids[p] = e;
+        if (e < 0 || e >= E) s_bad = 1;
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (threadIdx.x == 0) {
+            hdr[0] = QSTATUS_BAD_EXPERT_ID;
+            hdr[1] = 0;
+            hdr[2] = P;
+            if (status_dev) *status_dev = QSTATUS_BAD_EXPERT_ID;
+        }
+        return;
+    }
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = s_ids[p];
+        int pos = 0;
+        for (int q = 0; q < P; q++) {
+            const int eq = s_ids[q];
+            pos += (eq < e) || (eq == e && q < p);
+        }
+        s_sorted[pos] = e;
+        pair_tok[pos] = p / k;
+        pair_of[p] = pos;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int nb = 0;
+        for (int pos = 0; pos < P;) {
+            const int e = s_sorted[pos];
+            int n = 1;
+            while (pos + n < P && s_sorted[pos + n] == e && n < smax) n++;
+            batches[nb++] = make_int4(e, pos, n, 0);
+            pos += n;
+        }
+        hdr[0] = QSTATUS_OK;
+        hdr[1] = nb;
+        hdr[2] = P;
+        if (status_dev) *status_dev = QSTATUS_OK;
+    }
+}
+
+// out[t][d] = sum_{r < k} w[t][r] * z[pair_of[t k + r]][d], in rank order.
+__global__ void k_expert_combine(const float* __restrict__ wts, int k, int D, const unsigned char* ws, WsLayout L,
+                                 float* __restrict__ out)
+{
+    const int t = blockIdx.y;
+    const int d = blockIdx.x * blockDim.x + threadIdx.x;
+    if (d >= D) return;
+    const int32_t* hdr = reinterpret_cast<const int32_t*>(ws + L.hdr);
+    const int32_t* pair_of = reinterpret_cast<const int32_t*>(ws + L.pair_of);
+    const float* z = reinterpret_cast<const float*>(ws + L.z);
+    float acc = 0.0f;
+    if (hdr[0] == QSTATUS_OK) {
+        for (int r = 0; r < k; r++)
+            acc = fmaf(wts[t * k + r], z[(long long)pair_of[t * k + r] * D + d], acc);
+    }
+    out[(long long)t * D + d] = acc;
+}
+
+cudaError_t expert_prep(const ExpertArgs& a, cudaStream_t st)
+{
+    const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
+    k_expert_prep<<<1, 1024, 0, st>>>(a.ids, a.s * a.k, a.k, a.E, a.smax, a.ws, L, a.status_dev);
+    return cudaGetLastError();
+}
+
+cudaError_t expert_combine(const ExpertArgs& a, cudaStream_t st)
+{
+    const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
+    dim3 grid((a.D + 255) / 256, a.s);
+    k_expert_combine<<<grid, 256, 0, st>>>(a.wts, a.k, a.D, a.ws, L, a.out);
+    return cudaGetLastError();
+}
+
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+const char* qstatus_string(int status)
+{
+    switch (status) {
+    case QSTATUS_OK: return "ok";
+    case QSTATUS_BAD_FMT: return "unknown weight format, or a group size that format does not allow";
+    case QSTATUS_BAD_DIM: return "a size is out of range or not the multiple its format needs";
+    case QSTATUS_MISALIGNED: return "a pointer lacks the required alignment (16 B for packed weights and "
+                                    "activations, 4 B for scales and outputs)";
+    case QSTATUS_NULL: return "a required pointer is NULL";
+    case QSTATUS_WORKSPACE: return "workspace smaller than qexpert_group_workspace()";
+    case QSTATUS_LAUNCH: return "CUDA reported an error at launch (see qlast_cuda_error)";
+    case QSTATUS_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case QSTATUS_BAD_EXPERT_ID: return "an expert id is outside [0, E)";
+    default: return "unknown status";
+    }
+}
+
+const char* qlast_cuda_error(void) { return g_last_cuda_error; }
+
+int qgemv(int fmt, int gs, const void* w, const float* scales, const float* x, int O, int I, int s, float* y,
+          void* stream)
+{
+    int g = 0;
+    int st = check_fmt(fmt, gs, I, &g);
+    if (st) return st;
+    if (O < 1 || I < 1 || s < 1 || I > kMaxI) return QSTATUS_BAD_DIM;
+    if (!w || !scales || !x || !y) return QSTATUS_NULL;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(scales, 4) || !aligned(y, 4)) return QSTATUS_MISALIGNED;
+    int status = QSTATUS_OK;
+    const int grid = sm_count(&status);
+    if (status) return status;
+    const HostMat m{w, scales, O, I, g};
+    const int per = rows_per_launch(I);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    for (int s0 = 0; s0 < s; s0 += per) {
+        const int n = s - s0 < per ? s - s0 : per;
+        const float* xs = x + (size_t)s0 * I;
+        float* ys = y + (size_t)s0 * O;
+        cudaError_t e;
+#define QG_CALL(name) gemv_##name(m, xs, n, ys, O, grid, cs)
+        QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return QSTATUS_OK;
+}
+
+int qgate_up(int fmt, int gs, const void* wg, const float* sg, const void* wu, const float* su, const float* x,
+             int F, int D, int s, float* h, void* stream)
+{
+    int g = 0;
+    int st = check_fmt(fmt, gs, D, &g);
+    if (st) return st;
+    if (F < 1 || D < 1 || s < 1 || D > kMaxI) return QSTATUS_BAD_DIM;
+    if (!wg || !sg || !wu || !su || !x || !h) return QSTATUS_NULL;
+    if (!aligned(wg, 16) || !aligned(wu, 16) || !aligned(x, 16) || !aligned(sg, 4) || !aligned(su, 4) ||
+        !aligned(h, 4))
+        return QSTATUS_MISALIGNED;
+    int status = QSTATUS_OK;
+    const int grid = sm_count(&status);
+    if (status) return status;
+    const HostMat mg{wg, sg, F, D, g}, mu{wu, su, F, D, g};
+    const int per = rows_per_launch(D);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    for (int s0 = 0; s0 < s; s0 += per) {
+        const int n = s - s0 < per ? s - s0 : per;
+        cudaError_t e;
+#define QG_CALL(name) gate_up_##name(mg, mu, x + (size_t)s0 * D, n, h + (size_t)s0 * F, F, grid, cs)
+        QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    return QSTATUS_OK;
+}
+
+size_t qexpert_group_workspace(int E, int D, int F, int s, int k)
+{
+    (void)E;
+    if (D < 1 || F < 1 || s < 1 || k < 1) return 0;
+    return ws_layout(D, F, s, k).total;
+}
+
+int qexpert_group(int fmt, int gs, const void* gate, const float* gate_s, const void* up, const float* up_s,
+                  const void* down, const float* down_s, int E, int D, int F, const float* x, int s, int k,
+                  const int32_t* ids, const float* wts, float* out, void* workspace, size_t ws_bytes,
+                  int32_t* status_dev, void* stream)
+{
+    int g_up = 0, g_dn = 0;
+    int st = check_fmt(fmt, gs, D, &g_up);
+    if (st) return st;
+    st = check_fmt(fmt, gs, F, &g_dn);
+    if (st) return st;
+    if (E < 1 || D < 1 || F < 1 || s < 1 || k < 1 || D > kMaxI || F > kMaxI) return QSTATUS_BAD_DIM;
+    if ((long long)s * k > kMaxPairs) return QSTATUS_BAD_DIM;
+    if (!gate || !gate_s || !up || !up_s || !down || !down_s || !x || !ids || !wts || !out || !workspace)
+        return QSTATUS_NULL;
+    if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(down, 16) || !aligned(x, 16) ||
+        !aligned(workspace, 256) || !aligned(gate_s, 4) || !aligned(up_s, 4) || !aligned(down_s, 4) ||
+        !aligned(ids, 4) || !aligned(wts, 4) || !aligned(out, 4) || (status_dev && !aligned(status_dev, 4)))
+        return QSTATUS_MISALIGNED;
+    if (ws_bytes < ws_layout(D, F, s, k).total) return QSTATUS_WORKSPACE;
+    int status = QSTATUS_OK;
+    const int grid = sm_count(&status);
+    if (status) return status;
+
+    ExpertArgs a;
+    a.gs = fmt == QFMT_INT8_ROW ? 0 : g_up;
+    a.gate = gate; a.up = up; a.down = down;
+    a.gate_s = gate_s; a.up_s = up_s; a.down_s = down_s;
+    a.E = E; a.D = D; a.F = F; a.s = s; a.k = k;
+    a.x = x; a.ids = ids; a.wts = wts; a.out = out;
+    a.ws = static_cast<unsigned char*>(workspace);
+    a.status_dev = status_dev;
+    const int big = D > F ? D : F;
+    a.smax = rows_per_launch(big);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+    cudaError_t e = expert_prep(a, cs);
+    if (e != cudaSuccess) return launch_status(e);
+#define QG_CALL(name) expert_up_##name(a, grid, cs)
+    QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+    if (e != cudaSuccess) return launch_status(e);
+#define QG_CALL(name) expert_down_##name(a, grid, cs)
+    QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+    if (e != cudaSuccess) return launch_status(e);
+    e = expert_combine(a, cs);
+    if (e != cudaSuccess) return launch_status(e);
+    return QSTATUS_OK;
+}
+
+int qdequant(int fmt, int gs, const void* w, const float* scales, int O, int I, float* out, void* stream)
+{
+    int g = 0;
+    int st = check_fmt(fmt, gs, I, &g);
+    if (st) return st;
+    if (O < 1 || I < 1) return QSTATUS_BAD_DIM;
+    if (!w || !scales || !out) return QSTATUS_NULL;
+    if (!aligned(w, 16) || !aligned(scales, 4) || !aligned(out, 4)) return QSTATUS_MISALIGNED;
+    const HostMat m{w, scales, O, I, g};
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+#define QG_CALL(name) dequant_##name(m, out, cs)
+    QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+    return launch_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,489 @@
+// qg_device.cuh -- device code shared by the quantized GEMV, the fused gate/up
+// and the routed-expert kernels (sm_103a).
+//
+// What is computed (colibri Vulkan guide, xdnf.cn, section 着色器层面的实现细节,
+// and its API section): y[s][o] = sum_i value(code[o][i]) * scale[o][i/gs] * x[s][i]
+// for int8 per row, int4 (nibble - 8), int3-g64 in two bit planes (code - 4)
+// and MXFP4 e2m1 nibbles, with f32 group scales.
+//
+// How (GB300-first):
+//  * One lane owns one 16-byte "chunk" of a row per step (int3: 16 B of plane A
+//    plus 8 B of plane B), loaded with 128-bit non-caching loads: a warp step
+//    reads 512 contiguous bytes of a row, fully coalesced.  int4, MXFP4 and
+//    int3 chunks are exactly one scale group, so a lane needs one scale per
+//    chunk.
+//  * x (or the expert hidden vectors) sits in shared memory once per CTA in a
+//    swizzled order: lane l's x segment is 64-256 contiguous bytes, so plain
+//    placement would make the 8 lanes of a 128-bit shared-memory wavefront hit
+//    the same banks; XOR-ing the 16-byte quad index with low bits of the chunk
+//    index spreads them over all 32 banks.
+//  * Codes become f32 without integer-to-float conversions: a code OR-ed into
+//    the mantissa of 2^23 is the float 2^23 + code (shifted left by 4k bits,
+//    2^23 + code * 16^k), and one subtraction of 2^23 + offset * 16^k gives
+//    (code - offset) * 16^k exactly.  Sums of each power-of-16 class go to
+//    their own accumulator and are rescaled (exactly) at the end of the chunk.
+//    MXFP4 uses the hardware e2m1x2 -> f16x2 conversion.
+//  * Packed f32x2 FMA/ADD halve the issue slots of the arithmetic.
+//  * Each warp streams R rows at a time through a P-deep ring of chunk
+//    registers, so P*R 16-byte loads per lane are in flight; finished row
+//    tiles are reduced across the warp with a transposed (reduce-scatter)
+//    butterfly, one shuffle per value instead of five.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qg {
+
+enum : int { FMT_INT8_ROW = 1, FMT_INT4_G = 4, FMT_INT3_G64 = 5, FMT_MXFP4_G32 = 7 };
+
+// Elements a lane decodes per chunk.
+template <int FMT> struct Traits;
+template <> struct Traits<FMT_INT8_ROW>  { static constexpr int EPL = 16; };
+template <> struct Traits<FMT_INT4_G>    { static constexpr int EPL = 32; };
+template <> struct Traits<FMT_INT3_G64>  { static constexpr int EPL = 64; };
+template <> struct Traits<FMT_MXFP4_G32> { static constexpr int EPL = 32; };
+
+// ---------------------------------------------------------------------------
+// Swizzled placement of an activation vector in shared memory.
+// Element i lives in chunk q = i / EPL, quad j = (i % EPL) / 4.  The quad is
+// stored at (j ^ swz(q)) inside the chunk's segment.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int x_swz(int EPL, int q) { return EPL == 16 ? ((q >> 1) & 3) : (q & 7); }
+
+// Physical float4 index of logical quad qd (= i / 4).
+__device__ __forceinline__ int x_quad_phys(int EPL, int qd)
+{
+    const int qpc = EPL / 4;       // quads per chunk
+    const int q = qd / qpc;
+    const int j = qd - q * qpc;
+    return q * qpc + (j ^ x_swz(EPL, q));
+}
+
+// ---------------------------------------------------------------------------
+// Packed f32x2 helpers (sm_100+ PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// ---------------------------------------------------------------------------
+// Global loads of streamed weights: read once, keep out of L1.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ldg_stream16(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg_stream8(const void* p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ldg_f32(const float* p)
+{
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// A weight matrix as the kernels see it.
+// ---------------------------------------------------------------------------
+struct Mat {
+    const uint8_t* w;      // packed codes (int3: plane A, then plane B)
+    const float* sc;       // scales [O][I/gs]
+    long long O;           // rows
+    int I;                 // inputs per row
+    int ngrp;              // scale groups per row (I/gs; int8: 1)
+    int gsh;               // chunk -> group shift (int4: log2(gs/32)); else 0
+};
+
+template <int FMT> struct Chunk { uint4 w; };
+template <> struct Chunk<FMT_INT3_G64> { uint4 a; uint2 b; };
+
+template <int FMT>
+__device__ __forceinline__ void load_chunk(const Mat& m, long long o, int q, Chunk<FMT>& c, float& sc)
+{
+    if constexpr (FMT == FMT_INT8_ROW) {
+        c.w = ldg_stream16(m.w + o * m.I + (long long)q * 16);
+        sc = ldg_f32(m.sc + o);
+    } else if constexpr (FMT == FMT_INT3_G64) {
+        const long long rowA = (long long)(m.I / 4), rowB = (long long)(m.I / 8);
+        c.a = ldg_stream16(m.w + o * rowA + (long long)q * 16);
+        c.b = ldg_stream8(m.w + m.O * rowA + o * rowB + (long long)q * 8);
+        sc = ldg_f32(m.sc + o * m.ngrp + q);
+    } else {
+        c.w = ldg_stream16(m.w + o * (long long)(m.I / 2) + (long long)q * 16);
+        sc = ldg_f32(m.sc + o * m.ngrp + (q >> m.gsh));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Decoding.  A code c OR-ed into the mantissa of a float whose exponent is
+// chosen for the code's bit position gives 2^e + c exactly; subtracting
+// 2^e + offset gives c - offset.  int4 nibble k of a 16-bit half sits at bits
+// 4k..4k+3, so its float is ((150 - 4k) << 23) | (w & (0xF << 4k)) =
+// 2^(23-4k) + c.  Bytes (int8, int3 codes gathered into bytes) are moved under
+// 2^23 with one byte permute.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kMag0 = 0x4B000000u;   // 2^23, code at bits 0..
+constexpr uint32_t kMag1 = 0x49000000u;   // 2^19, code at bits 4..
+constexpr uint32_t kMag2 = 0x47000000u;   // 2^15, code at bits 8..
+constexpr uint32_t kMag3 = 0x45000000u;   // 2^11, code at bits 12..
+
+// int4 word (elements 8j..8j+7: low nibble first) -> four value pairs.
+__device__ __forceinline__ void decode_int4_word(uint32_t v, float2 (&d)[4])
+{
+    const float2 B01 = make_float2(-8388616.0f, -524296.0f);   // -(2^23 + 8), -(2^19 + 8)
+    const float2 B23 = make_float2(-32776.0f, -2056.0f);       // -(2^15 + 8), -(2^11 + 8)
+    const uint32_t h = v >> 16;
+    d[0] = fadd2(make_float2(u2f((v & 0x000Fu) | kMag0), u2f((v & 0x00F0u) | kMag1)), B01);
+    d[1] = fadd2(make_float2(u2f((v & 0x0F00u) | kMag2), u2f((v & 0xF000u) | kMag3)), B23);
+    d[2] = fadd2(make_float2(u2f((h & 0x000Fu) | kMag0), u2f((h & 0x00F0u) | kMag1)), B01);
+    d[3] = fadd2(make_float2(u2f((h & 0x0F00u) | kMag2), u2f((h & 0xF000u) | kMag3)), B23);
+}
+
+// int8 word (elements 4j..4j+3) -> two value pairs.  b ^ 0x80 = b + 128.
+__device__ __forceinline__ void decode_int8_word(uint32_t v, float2 (&d)[2])
+{
+    const float2 B = make_float2(-8388736.0f, -8388736.0f);    // -(2^23 + 128)
+    v ^= 0x80808080u;
+    d[0] = fadd2(make_float2(u2f(__byte_perm(v, kMag0, 0x7440)), u2f(__byte_perm(v, kMag0, 0x7441))), B);
+    d[1] = fadd2(make_float2(u2f(__byte_perm(v, kMag0, 0x7442)), u2f(__byte_perm(v, kMag0, 0x7443))), B);
+}
+
+// MXFP4: one byte = two e2m1 codes (low nibble first) -> f32 pair, through the
+// hardware e2m1x2 -> f16x2 conversion.
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte_in_low_bits)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\t.reg .b16 u;\n\tcvt.u16.u32 u, %1;\n\tcvt.u8.u16 t, u;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h2) : "r"(byte_in_low_bits));
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+__device__ __forceinline__ void decode_mxfp4_word(uint32_t v, float2 (&d)[4])
+{
+    d[0] = e2m1x2_to_f32x2(v);
+    d[1] = e2m1x2_to_f32x2(v >> 8);
+    d[2] = e2m1x2_to_f32x2(v >> 16);
+    d[3] = e2m1x2_to_f32x2(v >> 24);
+}
+
+// int3-g64: plane A word j holds the low two bits of elements 16j..16j+15
+// (two bits each, least significant first); the matching 16 bits of plane B
+// hold their high bits.  Elements 16j + 4m + r are gathered per class r into
+// byte m of word c[r] as a clean 3-bit code.
+__device__ __forceinline__ void int3_classes(uint32_t A, uint32_t bhalf, uint32_t (&c)[4])
+{
+    uint32_t t = bhalf & 0xFFFFu;
+    t = (t | (t << 8)) & 0x00FF00FFu;       // nibble m -> byte m
+    t = (t | (t << 4)) & 0x0F0F0F0Fu;
+    c[0] = (A & 0x03030303u) | ((t << 2) & 0x04040404u);
+    c[1] = ((A >> 2) & 0x03030303u) | ((t << 1) & 0x04040404u);
+    c[2] = ((A >> 4) & 0x03030303u) | (t & 0x04040404u);
+    c[3] = ((A >> 6) & 0x03030303u) | ((t >> 1) & 0x04040404u);
+}
+
+// Elements 16j + 4m + 0..3 (quad 4j + m) -> two value pairs (code - 4).
+__device__ __forceinline__ void decode_int3_quad(const uint32_t (&c)[4], int m, float2 (&d)[2])
+{
+    const float2 B = make_float2(-8388612.0f, -8388612.0f);    // -(2^23 + 4)
+    const uint32_t sel = 0x7440u + (uint32_t)m;
+    d[0] = fadd2(make_float2(u2f(__byte_perm(c[0], kMag0, sel)), u2f(__byte_perm(c[1], kMag0, sel))), B);
+    d[1] = fadd2(make_float2(u2f(__byte_perm(c[2], kMag0, sel)), u2f(__byte_perm(c[3], kMag0, sel))), B);
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int j)
+{
+    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// ---------------------------------------------------------------------------
+// Chunk consumption: for NR chunk rows (one chunk each) and S activation rows,
+// acc[rr][s] += scale[rr] * sum_chunk value(code) * x_s.  Word-major order
+// keeps only one word's decoded values and one x quad pair live at a time.
+// xb[s] points at the chunk's swizzled x segment; xo[j] = 4 * (j ^ swz).
+// ---------------------------------------------------------------------------
+template <int FMT, int S, int NR>
+__device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (&sc)[NR],
+                                        const float* const (&xb)[S], const int (&xo)[8], float (&acc)[NR][S])
+{
+    float2 part[NR][S];
+#pragma unroll
+    for (int rr = 0; rr < NR; rr++)
+#pragma unroll
+        for (int s = 0; s < S; s++) part[rr][s] = make_float2(0.f, 0.f);
+
+    if constexpr (FMT == FMT_INT4_G || FMT == FMT_MXFP4_G32) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            float2 d[NR][4];
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) {
+                if constexpr (FMT == FMT_INT4_G) decode_int4_word(word(c[rr].w, j), d[rr]);
+                else decode_mxfp4_word(word(c[rr].w, j), d[rr]);
+            }
+#pragma unroll
+            for (int s = 0; s < S; s++) {
+                const float4 xa = lds4(xb[s] + xo[2 * j]);
+                const float4 xc = lds4(xb[s] + xo[2 * j + 1]);
+#pragma unroll
+                for (int rr = 0; rr < NR; rr++) {
+                    part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
+                    part[rr][s] = ffma2(d[rr][1], make_float2(xa.z, xa.w), part[rr][s]);
+                    part[rr][s] = ffma2(d[rr][2], make_float2(xc.x, xc.y), part[rr][s]);
+                    part[rr][s] = ffma2(d[rr][3], make_float2(xc.z, xc.w), part[rr][s]);
+                }
+            }
+        }
+    } else if constexpr (FMT == FMT_INT8_ROW) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            float2 d[NR][2];
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) decode_int8_word(word(c[rr].w, j), d[rr]);
+#pragma unroll
+            for (int s = 0; s < S; s++) {
+                const float4 xa = lds4(xb[s] + xo[j]);
+#pragma unroll
+                for (int rr = 0; rr < NR; rr++) {
+                    part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
+                    part[rr][s] = ffma2(d[rr][1], make_float2(xa.z, xa.w), part[rr][s]);
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            uint32_t cls[NR][4];
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) {
+                const uint32_t bh = ((j & 2) ? c[rr].b.y : c[rr].b.x) >> ((j & 1) * 16);
+                int3_classes(word(c[rr].a, j), bh, cls[rr]);
+            }
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                float2 d[NR][2];
+#pragma unroll
+                for (int rr = 0; rr < NR; rr++) decode_int3_quad(cls[rr], m, d[rr]);
+                const int qd = 4 * j + m;
+#pragma unroll
+                for (int s = 0; s < S; s++) {
+                    const float4 xq = lds4(xb[s] + (qd >= 8 ? 32 : 0) + xo[qd & 7]);
+#pragma unroll
+                    for (int rr = 0; rr < NR; rr++) {
+                        part[rr][s] = ffma2(d[rr][0], make_float2(xq.x, xq.y), part[rr][s]);
+                        part[rr][s] = ffma2(d[rr][1], make_float2(xq.z, xq.w), part[rr][s]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < NR; rr++)
+#pragma unroll
+        for (int s = 0; s < S; s++) acc[rr][s] = fmaf(part[rr][s].x + part[rr][s].y, sc[rr], acc[rr][s]);
+}
+
+// ---------------------------------------------------------------------------
+// Stage activation rows into shared memory (swizzled, float4 granularity).
+// src[s] are f32 rows of length I (16-byte aligned); all threads take part.
+// ---------------------------------------------------------------------------
+template <int EPL>
+__device__ __forceinline__ void stage_rows(float* xs, int xstride, const float* const* src, int nrows, int I)
+{
+    const int nq = I / 4;
+    for (int idx = threadIdx.x; idx < nrows * nq; idx += blockDim.x) {
+        const int s = idx / nq;
+        const int qd = idx - s * nq;
+        const float4 v = *reinterpret_cast<const float4*>(src[s] + 4 * qd);
+        *reinterpret_cast<float4*>(xs + (long long)s * xstride + 4 * x_quad_phys(EPL, qd)) = v;
+    }
+}
+
+__host__ __device__ constexpr int ilog2(int v) { int l = 0; while ((1 << l) < v) l++; return l; }
+
+// ---------------------------------------------------------------------------
+// Transposed warp reduction of V (power of two, <= 32) values: afterwards lane
+// l < V holds the sum over the warp of value idx(l), with
+// idx(l) = sum_k bit_k(l) * (V >> (k + 1)).
+// ---------------------------------------------------------------------------
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane)
+{
+    static_assert((V & (V - 1)) == 0 && V <= 32, "V must be a power of two <= 32");
+#pragma unroll
+    for (int k = 0, n = V; n > 1; k++, n >>= 1) {
+        const bool up = (lane >> k) & 1;
+#pragma unroll
+        for (int i = 0; i < n / 2; i++) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << k);
+        }
+    }
+    float r = v[0];
+    constexpr int logv = ilog2(V);
+#pragma unroll
+    for (int k = logv; k < 5; k++) r += __shfl_xor_sync(0xffffffffu, r, 1 << k);
+    return r;
+}
+
+template <int V>
+__device__ __forceinline__ int reduce_scatter_index(int lane)
+{
+    int idx = 0;
+#pragma unroll
+    for (int k = 0; (V >> (k + 1)) > 0; k++)
+        if ((lane >> k) & 1) idx += V >> (k + 1);
+    return idx;
+}
+
+__host__ __device__ constexpr int pow2_ceil(int v) { int p = 1; while (p < v) p <<= 1; return p; }
+
+// ---------------------------------------------------------------------------
+// Row streaming.  A warp processes row tiles of R rows (of NM matrices sharing
+// the same row index: NM = 2 for gate and up).  Tiles tile_first,
+// tile_first + tile_step, ... below ntiles, rows row0 + tile * R + r < row_end.
+// Work is the flattened sequence (tile, step); step c covers chunk c*32 + lane.
+// The sink is called once per finished tile from every lane:
+//   sink(lane_idx_value, value_index, valid_lane) where value index
+//   v = (s * R + r) * NM + m.
+// ---------------------------------------------------------------------------
+template <int FMT, int S, int R, int P, int NM>
+struct RowStreamer {
+    static constexpr int EPL = Traits<FMT>::EPL;
+    static constexpr int V = pow2_ceil(S * R * NM);
+
+    Chunk<FMT> slot[P][NM * R];
+    float ssc[P][NM * R];
+    int it_tile, it_c;      // issue pointer
+    int ct_tile, ct_c;      // consume pointer
+    int total, done;
+
+    Mat mats[NM];
+    long long row0, row_end;
+    int nchunks, nsteps, tile_step, lane;
+
+    __device__ __forceinline__ void issue(int p)
+    {
+        const int q = it_c * 32 + lane;
+        const bool ok = q < nchunks;
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            long long o = row0 + (long long)it_tile * R + r;
+            o = o < row_end ? o : row_end - 1;       // tail rows: load a valid row, drop the result
+#pragma unroll
+            for (int m = 0; m < NM; m++) {
+                if (ok) load_chunk<FMT>(mats[m], o, q, slot[p][m * R + r], ssc[p][m * R + r]);
+            }
+        }
+        if (++it_c == nsteps) { it_c = 0; it_tile += tile_step; }
+    }
+
+    __device__ __forceinline__ void begin(const Mat* m, long long row0_, long long row_end_, int tile_first,
+                                          int ntiles, int tile_step_, int lane_)
+    {
+#pragma unroll
+        for (int k = 0; k < NM; k++) mats[k] = m[k];
+        row0 = row0_;
+        row_end = row_end_;
+        lane = lane_;
+        tile_step = tile_step_;
+        nchunks = m[0].I / EPL;
+        nsteps = (nchunks + 31) / 32;
+        const int my_tiles = tile_first < ntiles ? (ntiles - tile_first + tile_step - 1) / tile_step : 0;
+        total = my_tiles * nsteps;
+        it_tile = ct_tile = tile_first;
+        it_c = ct_c = 0;
+        done = 0;
+#pragma unroll
+        for (int p = 0; p < P; p++)
+            if (p < total) issue(p);
+    }
+
+    // xbase[s]: swizzled x rows (token slots) in shared memory.
+    template <class Sink>
+    __device__ __forceinline__ void run(const float* const (&xbase)[S], Sink& sink)
+    {
+        const int swz = x_swz(EPL, lane);
+        int xo[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) xo[j] = 4 * (j ^ swz);
+
+        float acc[NM * R][S];
+#pragma unroll
+        for (int rr = 0; rr < NM * R; rr++)
+#pragma unroll
+            for (int s = 0; s < S; s++) acc[rr][s] = 0.f;
+
+        for (int j0 = 0; j0 < total; j0 += P) {
+#pragma unroll
+            for (int p = 0; p < P; p++) {
+                if (j0 + p < total) {
+                    const int q = ct_c * 32 + lane;
+                    if (q < nchunks) {
+                        const float* xb[S];
+#pragma unroll
+                        for (int s = 0; s < S; s++) xb[s] = xbase[s] + q * EPL;
+                        consume<FMT, S, NM * R>(slot[p], ssc[p], xb, xo, acc);
+                    }
+                    if (j0 + p + P < total) issue(p);
+                    if (++ct_c == nsteps) {
+                        // finished tile ct_tile: reduce and hand to the sink
+                        float v[V];
+#pragma unroll
+                        for (int i = 0; i < V; i++) v[i] = 0.f;
+#pragma unroll
+                        for (int s = 0; s < S; s++)
+#pragma unroll
+                            for (int r = 0; r < R; r++)
+#pragma unroll
+                                for (int m = 0; m < NM; m++) {
+                                    v[(s * R + r) * NM + m] = acc[m * R + r][s];
+                                    acc[m * R + r][s] = 0.f;
+                                }
+                        const float red = warp_reduce_scatter<V>(v, lane);
+                        const int idx = reduce_scatter_index<V>(lane);
+                        sink(red, idx, lane < V, row0 + (long long)ct_tile * R, row_end);
+                        ct_c = 0;
+                        ct_tile += tile_step;
+                    }
+                }
+            }
+        }
+    }
+};
+
+}  // namespace qg

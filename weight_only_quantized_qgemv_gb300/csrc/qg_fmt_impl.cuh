@@ -1,0 +1,435 @@
+// qg_fmt_impl.cuh -- the streaming kernels and their launchers for one weight
+// format.  Included by qg_fmt_<format>.cu with QG_FMT (format id) and QG_NAME
+// (launcher suffix) defined, so the four formats compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "qg_device.cuh"
+#include "qg_internal.h"
+
+#ifndef QG_FMT
+#error "define QG_FMT and QG_NAME before including qg_fmt_impl.cuh"
+#endif
+
+#define QG_CAT2(a, b) a##b
+#define QG_CAT(a, b) QG_CAT2(a, b)
+
+namespace qg {
+namespace QG_CAT(fmt_, QG_NAME) {
+
+constexpr int FMT = QG_FMT;
+constexpr int EPL = Traits<FMT>::EPL;
+
+// Rows per warp tile: up to 4 chunk rows (NM matrices x R rows) so each x
+// quad read from shared memory serves several rows, and at most 8
+// accumulators (S x NM x R) so everything stays in registers.
+// int3 chunks take 7 registers instead of 5, so their budget is 4
+// accumulators beyond the single-row-set case.
+template <int S, int NM>
+__host__ __device__ constexpr int rows_per_tile()
+{
+    constexpr int acc_budget = (FMT == FMT_INT3_G64 && S * NM > 1) ? 4 : 8;
+    constexpr int by_acc = acc_budget / (S * NM) > 0 ? acc_budget / (S * NM) : 1;
+    return (4 / NM) < by_acc ? (4 / NM) : by_acc;
+}
+
+constexpr int kRing = 2;   // chunk-register ring depth
+
+inline Mat to_mat(const HostMat& h)
+{
+    Mat m;
+    m.w = static_cast<const uint8_t*>(h.w);
+    m.sc = h.sc;
+    m.O = h.O;
+    m.I = h.I;
+    m.ngrp = FMT == FMT_INT8_ROW ? 1 : h.I / h.gs;
+    int sh = 0;
+    if (FMT == FMT_INT4_G) while ((32 << sh) < h.gs) sh++;
+    m.gsh = sh;
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// Jobs: where rows, activations and results of a streaming launch live.
+// ---------------------------------------------------------------------------
+
+// One matrix (or a gate/up pair) against s <= 8 activation rows.
+template <int NM>
+struct DenseJob {
+    Mat m[NM];
+    const float* x;      // [S][I]
+    float* y;            // y[s * ldy + row]
+    long long ldy;
+    int S;
+
+    __device__ bool bad() const { return false; }
+    __device__ int nbatch() const { return 1; }
+    __device__ long long rows_per() const { return m[0].O; }
+    __device__ int batch_S(int) const { return S; }
+    __device__ void mats(int, Mat (&out)[NM]) const
+    {
+#pragma unroll
+        for (int k = 0; k < NM; k++) out[k] = m[k];
+    }
+    __device__ const float* xrow(int, int s) const { return x + (long long)s * m[0].I; }
+    __device__ void store(int, int s, long long row, float v) const { y[(long long)s * ldy + row] = v; }
+};
+
+// Expert phase A: the gate and up rows of every used expert, against the
+// tokens routed to it; stores h = silu(g) * u per sorted pair.
+struct ExpertUpJob {
+    Mat gate0, up0;                 // expert 0's matrices (w, sc advanced per expert)
+    long long mat_bytes, mat_scales;
+    const float* x;
+    const int32_t* hdr;
+    const int4* batches;
+    const int32_t* pair_tok;
+    float* h;
+    int D, F;
+
+    __device__ bool bad() const { return hdr[0] != 0; }
+    __device__ int nbatch() const { return hdr[1]; }
+    __device__ long long rows_per() const { return F; }
+    __device__ int batch_S(int b) const { return batches[b].z; }
+    __device__ void mats(int b, Mat (&out)[2]) const
+    {
+        const long long e = batches[b].x;
+        out[0] = gate0;
+        out[0].w += e * mat_bytes;
+        out[0].sc += e * mat_scales;
+        out[1] = up0;
+        out[1].w += e * mat_bytes;
+        out[1].sc += e * mat_scales;
+    }
+    __device__ const float* xrow(int b, int s) const { return x + (long long)pair_tok[batches[b].y + s] * D; }
+    __device__ void store(int b, int s, long long row, float v) const
+    {
+        h[(long long)(batches[b].y + s) * F + row] = v;
+    }
+};
+
+// Expert phase B: the down rows of every used expert against the h vectors of
+// its pairs; stores z = down h per sorted pair.
+struct ExpertDownJob {
+    Mat down0;
+    long long mat_bytes, mat_scales;
+    const int32_t* hdr;
+    const int4* batches;
+    const float* h;
+    float* z;
+    int D, F;
+
+    __device__ bool bad() const { return hdr[0] != 0; }
+    __device__ int nbatch() const { return hdr[1]; }
+    __device__ long long rows_per() const { return D; }
+    __device__ int batch_S(int b) const { return batches[b].z; }
+    __device__ void mats(int b, Mat (&out)[1]) const
+    {
+        const long long e = batches[b].x;
+        out[0] = down0;
+        out[0].w += e * mat_bytes;
+        out[0].sc += e * mat_scales;
+    }
+    __device__ const float* xrow(int b, int s) const { return h + (long long)(batches[b].y + s) * F; }
+    __device__ void store(int b, int s, long long row, float v) const
+    {
+        z[(long long)(batches[b].y + s) * D + row] = v;
+    }
+};
+
+// Hands finished tiles to the job (NM = 2: h = silu(gate) * up).
+template <class Job, int S, int R, int NM>
+struct Sink {
+    const Job& job;
+    int b;
+    __device__ __forceinline__ void operator()(float v, int idx, bool lane_ok, long long tile_row0,
+                                               long long row_end) const
+    {
+        constexpr int V = pow2_ceil(S * R * NM);
+        if constexpr (NM == 2) {
+            const float u = __shfl_xor_sync(0xffffffffu, v, V / 2);
+            if (lane_ok && !(idx & 1) && idx < S * R * 2) {
+                const int sr = idx >> 1, s = sr / R, r = sr - (sr / R) * R;
+                const long long row = tile_row0 + r;
+                if (row < row_end) job.store(b, s, row, v / (1.0f + expf(-v)) * u);
+            }
+        } else {
+            if (lane_ok && idx < S * R) {
+                const int s = idx / R, r = idx - (idx / R) * R;
+                const long long row = tile_row0 + r;
+                if (row < row_end) job.store(b, s, row, v);
+            }
+        }
+    }
+};
+
+// One segment: rows [l0, l1) of batch b, all warps of the CTA.  Not inlined,
+// so a kernel that dispatches over several S gets a register allocation per S.
+template <int NM, int S, class Job>
+__device__ __noinline__ void segment(const Job job, int b, long long l0, long long l1, float* xs, int& staged)
+{
+    constexpr int R = rows_per_tile<S, NM>();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Mat m[NM];
+    job.mats(b, m);
+    const int ntiles = (int)((l1 - l0 + R - 1) / R);
+    RowStreamer<FMT, S, R, kRing, NM> st;
+    st.begin(m, l0, l1, warp, ntiles, kWarps, lane);      // weight loads in flight during staging
+    const int I = m[0].I;
+    if (b != staged) {
+        __syncthreads();
+        const float* src[S];
+#pragma unroll
+        for (int s = 0; s < S; s++) src[s] = job.xrow(b, s);
+        stage_rows<EPL>(xs, I, src, S, I);
+        __syncthreads();
+        staged = b;
+    }
+    const float* xb[S];
+#pragma unroll
+    for (int s = 0; s < S; s++) xb[s] = xs + (long long)s * I;
+    Sink<Job, S, R, NM> sink{job, b};
+    st.run(xb, sink);
+}
+
+template <int NM, int S, int SMAX, class Job>
+__device__ __forceinline__ void segment_dispatch(int Sr, const Job& job, int b, long long l0, long long l1,
+                                                 float* xs, int& staged)
+{
+    if constexpr (S <= SMAX) {
+        if (Sr == S) segment<NM, S>(job, b, l0, l1, xs, staged);
+        else segment_dispatch<NM, S + 1, SMAX>(Sr, job, b, l0, l1, xs, staged);
+    }
+}
+
+// The streaming kernel: CTA c takes the rows [N c / G, N (c+1) / G) of the
+// job's batches laid end to end (N = batches * rows per batch), so every SM
+// gets the same number of weight rows; the range splits into segments where
+// the batch (and so the staged activation set) changes.
+template <int NM, int SMIN, int SMAX, class Job>
+__global__ void __launch_bounds__(kThreads, 1) k_stream(const Job job)
+{
+    extern __shared__ float4 qg_smem4[];
+    float* xs = reinterpret_cast<float*>(qg_smem4);
+    if (job.bad()) return;
+    const long long rows_per = job.rows_per();
+    const long long N = (long long)job.nbatch() * rows_per;
+    const long long r_begin = N * blockIdx.x / gridDim.x;
+    const long long r_end = N * (blockIdx.x + 1) / gridDim.x;
+    int staged = -1;
+    long long r = r_begin;
+    while (r < r_end) {
+        const int b = (int)(r / rows_per);
+        const long long base = (long long)b * rows_per;
+        const long long l0 = r - base;
+        const long long l1 = (r_end - base) < rows_per ? (r_end - base) : rows_per;
+        const int S = job.batch_S(b);
+        segment_dispatch<NM, SMIN, SMAX>(S, job, b, l0, l1, xs, staged);
+        r = base + l1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dequantization: one thread per chunk, the same decoding arithmetic as the
+// dot products, then one f32 multiplication by the scale.
+// ---------------------------------------------------------------------------
+template <int F_>
+__device__ __forceinline__ void decode_chunk(const Chunk<F_>& c, float* v)
+{
+    if constexpr (F_ == FMT_INT4_G || F_ == FMT_MXFP4_G32) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            float2 d[4];
+            if constexpr (F_ == FMT_INT4_G) decode_int4_word(word(c.w, j), d);
+            else decode_mxfp4_word(word(c.w, j), d);
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                v[8 * j + 2 * k] = d[k].x;
+                v[8 * j + 2 * k + 1] = d[k].y;
+            }
+        }
+    } else if constexpr (F_ == FMT_INT8_ROW) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            float2 d[2];
+            decode_int8_word(word(c.w, j), d);
+            v[4 * j + 0] = d[0].x;
+            v[4 * j + 1] = d[0].y;
+            v[4 * j + 2] = d[1].x;
+            v[4 * j + 3] = d[1].y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            uint32_t cls[4];
+            const uint32_t bh = ((j & 2) ? c.b.y : c.b.x) >> ((j & 1) * 16);
+            int3_classes(word(c.a, j), bh, cls);
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                float2 d[2];
+                decode_int3_quad(cls, m, d);
+                v[16 * j + 4 * m + 0] = d[0].x;
+                v[16 * j + 4 * m + 1] = d[0].y;
+                v[16 * j + 4 * m + 2] = d[1].x;
+                v[16 * j + 4 * m + 3] = d[1].y;
+            }
+        }
+    }
+}
+
+__global__ void k_dequant(const Mat m, float* __restrict__ out)
+{
+    const long long nchunks = (long long)(m.I / EPL);
+    const long long total = m.O * nchunks;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long o = t / nchunks;
+        const int q = (int)(t - o * nchunks);
+        Chunk<FMT> c;
+        float sc;
+        load_chunk<FMT>(m, o, q, c, sc);
+        float v[EPL];
+        decode_chunk<FMT>(c, v);
+        float* dst = out + o * m.I + (long long)q * EPL;
+#pragma unroll
+        for (int i = 0; i < EPL; i++) dst[i] = v[i] * sc;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers.
+// ---------------------------------------------------------------------------
+// Raises a kernel's dynamic shared-memory limit when a launch needs more than
+// it was last given (per device), so repeated calls -- and launches captured
+// into a CUDA graph after a first eager call -- make no attribute call.
+template <class K>
+static cudaError_t set_smem(K kernel, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    static int granted[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && granted[dev] >= (int)bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) granted[dev] = (int)bytes;
+    return e;
+}
+
+template <int NM, int S>
+static cudaError_t launch_dense(const DenseJob<NM>& job, int grid, size_t smem, cudaStream_t st)
+{
+    auto kern = k_stream<NM, S, S, DenseJob<NM>>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(job);
+    return cudaGetLastError();
+}
+
+template <int NM>
+static cudaError_t launch_dense_s(const DenseJob<NM>& job, int s, int grid, size_t smem, cudaStream_t st)
+{
+    switch (s) {
+    case 1: return launch_dense<NM, 1>(job, grid, smem, st);
+    case 2: return launch_dense<NM, 2>(job, grid, smem, st);
+    case 3: return launch_dense<NM, 3>(job, grid, smem, st);
+    case 4: return launch_dense<NM, 4>(job, grid, smem, st);
+    case 5: return launch_dense<NM, 5>(job, grid, smem, st);
+    case 6: return launch_dense<NM, 6>(job, grid, smem, st);
+    case 7: return launch_dense<NM, 7>(job, grid, smem, st);
+    case 8: return launch_dense<NM, 8>(job, grid, smem, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fmt_<name>
+
+using namespace QG_CAT(fmt_, QG_NAME);
+
+cudaError_t QG_CAT(gemv_, QG_NAME)(const HostMat& hm, const float* x, int s, float* y, long long ldy, int grid,
+                                   cudaStream_t st)
+{
+    DenseJob<1> job;
+    job.m[0] = to_mat(hm);
+    job.x = x;
+    job.y = y;
+    job.ldy = ldy;
+    job.S = s;
+    return launch_dense_s<1>(job, s, grid, (size_t)s * hm.I * sizeof(float), st);
+}
+
+cudaError_t QG_CAT(gate_up_, QG_NAME)(const HostMat& g, const HostMat& u, const float* x, int s, float* h,
+                                      long long ldh, int grid, cudaStream_t st)
+{
+    DenseJob<2> job;
+    job.m[0] = to_mat(g);
+    job.m[1] = to_mat(u);
+    job.x = x;
+    job.y = h;
+    job.ldy = ldh;
+    job.S = s;
+    return launch_dense_s<2>(job, s, grid, (size_t)s * g.I * sizeof(float), st);
+}
+
+cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st)
+{
+    const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
+    const int gs = FMT == FMT_INT8_ROW ? a.D : a.gs;
+    ExpertUpJob job;
+    job.gate0 = to_mat(HostMat{a.gate, a.gate_s, a.F, a.D, gs});
+    job.up0 = to_mat(HostMat{a.up, a.up_s, a.F, a.D, gs});
+    job.mat_bytes = FMT == FMT_INT8_ROW ? (long long)a.F * a.D
+                  : FMT == FMT_INT3_G64 ? (long long)a.F * a.D / 4 + (long long)a.F * a.D / 8
+                                        : (long long)a.F * a.D / 2;
+    job.mat_scales = (long long)a.F * (a.D / gs);
+    job.x = a.x;
+    job.hdr = reinterpret_cast<const int32_t*>(a.ws + L.hdr);
+    job.batches = reinterpret_cast<const int4*>(a.ws + L.batches);
+    job.pair_tok = reinterpret_cast<const int32_t*>(a.ws + L.pair_tok);
+    job.h = reinterpret_cast<float*>(a.ws + L.h);
+    job.D = a.D;
+    job.F = a.F;
+    auto kern = k_stream<2, 1, kSmax, ExpertUpJob>;
+    const size_t smem = (size_t)a.smax * a.D * sizeof(float);
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(job);
+    return cudaGetLastError();
+}
+
+cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st)
+{
+    const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
+    const int gs = FMT == FMT_INT8_ROW ? a.F : a.gs;
+    ExpertDownJob job;
+    job.down0 = to_mat(HostMat{a.down, a.down_s, a.D, a.F, gs});
+    job.mat_bytes = FMT == FMT_INT8_ROW ? (long long)a.D * a.F
+                  : FMT == FMT_INT3_G64 ? (long long)a.D * a.F / 4 + (long long)a.D * a.F / 8
+                                        : (long long)a.D * a.F / 2;
+    job.mat_scales = (long long)a.D * (a.F / gs);
+    job.hdr = reinterpret_cast<const int32_t*>(a.ws + L.hdr);
+    job.batches = reinterpret_cast<const int4*>(a.ws + L.batches);
+    job.h = reinterpret_cast<const float*>(a.ws + L.h);
+    job.z = reinterpret_cast<float*>(a.ws + L.z);
+    job.D = a.D;
+    job.F = a.F;
+    auto kern = k_stream<1, 1, kSmax, ExpertDownJob>;
+    const size_t smem = (size_t)a.smax * a.F * sizeof(float);
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(job);
+    return cudaGetLastError();
+}
+
+cudaError_t QG_CAT(dequant_, QG_NAME)(const HostMat& hm, float* out, cudaStream_t st)
+{
+    const Mat m = to_mat(hm);
+    const long long total = hm.O * (long long)(hm.I / EPL);
+    long long blocks = (total + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    k_dequant<<<(int)blocks, 256, 0, st>>>(m, out);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -58,10 +58,16 @@ def generator(seed: int, *spawn_key: int) -> np.random.Generator:
 
 
 def draw_packed(fmt: int, O: int, I: int, rng: np.random.Generator) -> np.ndarray:
-    """Packed weights with uniform codes (int8: uniform in [-127, 127])."""
+    """Packed weights with uniform codes (int8: uniform in [-127, 127]).
+
+    Uniform codes in every nibble, pair or bit are uniform bytes, which come
+    straight from the generator's raw 64-bit output.
+    """
     if fmt == INT8_ROW:
         return rng.integers(-127, 128, size=O * I, dtype=np.int8).view(np.uint8)
-    return rng.integers(0, 256, size=packed_bytes(fmt, O, I), dtype=np.uint8)
+    n = packed_bytes(fmt, O, I)
+    raw = rng.bit_generator.random_raw((n + 7) // 8).view(np.uint8)
+    return raw[:n].copy() if n % 8 else raw
 
 
 def draw_scales(O: int, I: int, gs: int, rng: np.random.Generator, kind: str,
@@ -69,7 +75,8 @@ def draw_scales(O: int, I: int, gs: int, rng: np.random.Generator, kind: str,
     """f32 scales [O][I/gs]: 'lognormal' (mu, sigma) or 'pow2' (2^k, k uniform in [-8, 0])."""
     n = O * (I // gs)
     if kind == "lognormal":
-        return rng.lognormal(mu, sigma, size=n).astype(np.float32)
+        z = rng.standard_normal(size=n, dtype=np.float32)
+        return np.exp(z * np.float32(sigma) + np.float32(mu)).astype(np.float32)
     if kind == "pow2":
         return np.ldexp(np.ones(n, dtype=np.float32), rng.integers(-8, 1, size=n)).astype(np.float32)
     raise ValueError(kind)
@@ -165,6 +172,46 @@ class ExpertWorkload:
         w = draw_packed(self.fmt, O, I, rng)
         sc = draw_scales(O, I, self.gs, rng, self.scale_kind, self.scale_mu)
         return w, sc
+
+    MATRICES = (("gate", 0), ("up", 1), ("down", 2))
+
+    def sizes(self, which: int):
+        """(packed bytes, scale count) of one expert matrix."""
+        O, I = self.matrix_shape(which)
+        return packed_bytes(self.fmt, O, I), O * (I // self.gs)
+
+    def generate(self, experts, sink, threads: int = 16):
+        """Draw the given experts' matrices in parallel, calling
+        sink(name, slot, packed, scales) for each (slot = position in `experts`)."""
+        from concurrent.futures import ThreadPoolExecutor
+        experts = [int(e) for e in experts]
+
+        def one(job):
+            slot, e, name, which = job
+            w, sc = self.expert_matrix(e, which)
+            sink(name, slot, w, sc)
+
+        jobs = [(slot, e, name, which) for name, which in self.MATRICES for slot, e in enumerate(experts)]
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, jobs))
+
+    def store(self, experts=None, threads: int = 16):
+        """{gate, gate_s, up, up_s, down, down_s}: the given experts (all by
+        default) back to back, in host memory."""
+        experts = list(range(self.E)) if experts is None else [int(e) for e in experts]
+        out = {}
+        for name, which in self.MATRICES:
+            nb, ns = self.sizes(which)
+            out[name] = np.empty(len(experts) * nb, dtype=np.uint8)
+            out[name + "_s"] = np.empty(len(experts) * ns, dtype=np.float32)
+
+        def sink(name, slot, w, sc):
+            nb, ns = w.size, sc.size
+            out[name][slot * nb:(slot + 1) * nb] = w
+            out[name + "_s"][slot * ns:(slot + 1) * ns] = sc
+
+        self.generate(experts, sink, threads)
+        return out
 
     def x(self, step: int = 0):
         return draw_x(self.s, self.D, generator(self.seed, 2, step))
