@@ -365,7 +365,8 @@ def reference_arm(args, wl, world, rank):
         return
     from oracle import oracle as orc
     orc.build()
-    run, desc = oracle_sample_runner(wl, target_s=max(0.5, 60.0 / max(1, args.steps + args.warmup)))
+    target = args.sample_seconds if args.sample_seconds else max(0.5, 60.0 / max(1, args.steps + args.warmup))
+    run, desc = oracle_sample_runner(wl, target_s=target)
     for i in range(args.warmup):
         run(i)
     t = time.perf_counter()
@@ -407,6 +408,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph-len", type=int, default=64, help="calls captured per CUDA graph replay")
+    ap.add_argument("--sample-seconds", type=float, default=None,
+                    help="CPU seconds per oracle sample (reference arm / CPU baseline)")
     args = ap.parse_args()
     wl = synth.workload(args.workload)
     world, rank, local = dist_env()
@@ -508,7 +511,7 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl)
+        cpu = cpu_baseline(wl, args.sample_seconds or 12.0)
     cfg = bench.config()
     cfg["graph_calls_per_replay"] = G
     line = {

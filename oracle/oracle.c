@@ -110,12 +110,23 @@ double oracle_code_value(int fmt, int code)
     }
 }
 
+/* Group size of a format: int8 per row has one group per row; int3-g64
+ * groups 64 inputs and MXFP4 32 ([GUIDE] shader details); int4 takes gs. */
+static long group_of(int fmt, long I, long gs)
+{
+    switch (fmt) {
+    case ORACLE_INT8_ROW: return I;
+    case ORACLE_INT3_G64: return 64;
+    case ORACLE_MXFP4_G32: return 32;
+    default: return gs;
+    }
+}
+
 /* The scale of element (o, i): one f32 per group of gs inputs along the row,
- * stored row-major [O][I/gs].  int8 per row has one group per row (gs = I). */
+ * stored row-major [O][I/gs]. */
 static double scale_of(int fmt, const float *scales, long I, long gs, long o, long i)
 {
-    if (fmt == ORACLE_INT8_ROW)
-        gs = I;
+    gs = group_of(fmt, I, gs);
     return (double)scales[o * (I / gs) + i / gs];
 }
 
@@ -221,9 +232,9 @@ void oracle_expert_group_cols(int fmt, long gs,
                               const long *cols, long ncols, double *out, double *h_scratch)
 {
     long gu_bytes = oracle_packed_bytes(fmt, F, D);
-    long gu_scales = (fmt == ORACLE_INT8_ROW) ? F : F * (D / gs);
+    long gu_scales = F * (D / group_of(fmt, D, gs));
     long dn_bytes = oracle_packed_bytes(fmt, D, F);
-    long dn_scales = (fmt == ORACLE_INT8_ROW) ? D : D * (F / gs);
+    long dn_scales = D * (F / group_of(fmt, F, gs));
     (void)E;
     for (long t = 0; t < s; t++) {
         for (long j = 0; j < ncols; j++)

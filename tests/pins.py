@@ -122,6 +122,19 @@ def pin_dequant_f32(orc):
             assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32)), f"fmt {fmt} gs {gs}"
 
 
+def pin_fixed_groups(orc):
+    """int3-g64 groups 64 inputs and MXFP4 32 whatever gs says; int8 one per row."""
+    rng = np.random.default_rng(12)
+    for fmt, g in ((INT3_G64, 64), (MXFP4_G32, 32), (INT8_ROW, 256)):
+        O, I = 2, 256
+        codes = random_codes(fmt, O, I, rng)
+        scales = rng.lognormal(-4, 1.0, size=O * (I // g)).astype(np.float32)
+        a = orc.dequant_f32(fmt, g, pack(fmt, codes), scales, O, I)
+        for other in (32, 64, 128):
+            b = orc.dequant_f32(fmt, other, pack(fmt, codes), scales, O, I)
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (fmt, other)
+
+
 # --- step a3: the GEMV -------------------------------------------------------
 
 def pin_gemv_bruteforce(orc):
@@ -290,5 +303,5 @@ def pin_expert_group(orc):
 
 
 ALL_PINS = [pin_e2m1, pin_int4_nibbles, pin_int3_planes, pin_int8_bytes, pin_random_codes,
-            pin_dequant_f32, pin_gemv_bruteforce, pin_zero_scales, pin_linearity, pin_integer_exact,
+            pin_dequant_f32, pin_fixed_groups, pin_gemv_bruteforce, pin_zero_scales, pin_linearity, pin_integer_exact,
             pin_silu, pin_gate_up, pin_expert_group]

@@ -57,7 +57,7 @@ def test_expert_group_small(fmt, gs, E, s, k):
     wts = rng.random((s, k)).astype(np.float32)
     out, status = run_group(fmt, gs, st, E, D, F, x, ids, wts)
     assert status == 0
-    want = oracle_group(fmt, gs or 32, st, E, D, F, x, ids, wts)
+    want = oracle_group(fmt, synth.fixed_group(fmt, D, gs or None), st, E, D, F, x, ids, wts)
     assert max_rel(out, want) <= GATE
 
 

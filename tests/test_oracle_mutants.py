@@ -24,6 +24,8 @@ MUTANTS = {
     "e2m1_no_sign": ("return sign ? -mag : mag;", "return mag;"),
     "e2m1_subnormal": ("(e == 0) ? 0.5 * m", "(e == 0) ? 1.0 * m"),
     "scale_first_group_only": ("scales[o * (I / gs) + i / gs]", "scales[o * (I / gs)]"),
+    "int3_group_32": ("case ORACLE_INT3_G64: return 64;", "case ORACLE_INT3_G64: return 32;"),
+    "mxfp4_group_64": ("case ORACLE_MXFP4_G32: return 32;", "case ORACLE_MXFP4_G32: return 64;"),
     "scale_group_mod": ("scales[o * (I / gs) + i / gs]", "scales[o * (I / gs) + i % (I / gs)]"),
     "gemv_dropped_term": ("for (long i = 0; i < I; i++)\n        acc +=", "for (long i = 1; i < I; i++)\n        acc +="),
     "gemv_token_ignored": ("y[t * O + o] = row_dot(fmt, gs, w, scales, O, I, o, x + t * I);",
