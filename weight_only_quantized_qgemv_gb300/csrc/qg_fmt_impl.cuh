@@ -303,11 +303,11 @@ __global__ void k_dequant(const Mat m, float* __restrict__ out)
 // Raises a kernel's dynamic shared-memory limit when a launch needs more than
 // it was last given (per device), so repeated calls -- and launches captured
 // into a CUDA graph after a first eager call -- make no attribute call.
+// `granted` is the calling launcher's own per-device record for `kernel`.
 template <class K>
-static cudaError_t set_smem(K kernel, size_t bytes)
+static cudaError_t set_smem(K kernel, size_t bytes, int (&granted)[64])
 {
     if (bytes <= 48 * 1024) return cudaSuccess;
-    static int granted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -321,7 +321,8 @@ template <int NM, int S>
 static cudaError_t launch_dense(const DenseJob<NM>& job, int grid, size_t smem, cudaStream_t st)
 {
     auto kern = k_stream<NM, S, S, DenseJob<NM>>;
-    cudaError_t e = set_smem(kern, smem);
+    static int granted[64];
+    cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(job);
     return cudaGetLastError();
@@ -392,7 +393,8 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
     job.F = a.F;
     auto kern = k_stream<2, 1, kSmax, ExpertUpJob>;
     const size_t smem = (size_t)a.smax * a.D * sizeof(float);
-    cudaError_t e = set_smem(kern, smem);
+    static int granted[64];
+    cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(job);
     return cudaGetLastError();
@@ -416,7 +418,8 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
     job.F = a.F;
     auto kern = k_stream<1, 1, kSmax, ExpertDownJob>;
     const size_t smem = (size_t)a.smax * a.F * sizeof(float);
-    cudaError_t e = set_smem(kern, smem);
+    static int granted[64];
+    cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(job);
     return cudaGetLastError();
