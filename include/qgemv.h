@@ -130,6 +130,37 @@ int qexpert_group(int fmt, int gs,
                   int32_t* status_dev, void* stream);
 
 /*
+ * qexpert_group for callers that cannot allocate device memory -- for
+ * example a plugin inside a host application that owns all of the GPU's
+ * memory through its own allocator and gives plugins no way to allocate, or a
+ * decode loop that must never allocate.  The pages have no counterpart: their
+ * backends allocate their own device buffers.
+ *
+ * Same arguments, result and status word as qexpert_group, without the
+ * workspace: the scratch is a fixed array of QEXPERT_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads the library holds
+ * until the process exits.  Sizes whose qexpert_group_workspace() exceeds it
+ * are rejected with QSTATUS_WORKSPACE before anything is enqueued.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call on a device shares the one array and leaves its
+ * contents behind; nothing in it needs clearing, since each call writes every
+ * scratch word it later reads.  Calls that overlap on the GPU (other streams,
+ * other host threads) race on the array: serialize them.
+ */
+#define QEXPERT_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+int qexpert_group_noalloc(int fmt, int gs,
+                          const void* gate, const float* gate_s,
+                          const void* up, const float* up_s,
+                          const void* down, const float* down_s,
+                          int E, int D, int F,
+                          const float* x, int s, int k,
+                          const int32_t* ids, const float* wts,
+                          float* out, int32_t* status_dev, void* stream);
+
+/*
  * out[o][i] = value(W[o][i]) * scales[o][i/gs] as f32 (one IEEE f32
  * multiplication of the exact code value by the scale).  For checking the
  * decoders bit for bit; out f32 [O][I].

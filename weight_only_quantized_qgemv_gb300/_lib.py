@@ -121,3 +121,15 @@ def qexpert_group(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, 
 
 def qdequant(fmt, gs, w, scales, O, I, out, stream=None):
     _check(lib().qdequant(fmt, gs, _ptr(w), _ptr(scales), O, I, _ptr(out), _stream(stream)))
+
+
+def qexpert_group_noalloc(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, out,
+                          status_dev=None, stream=None):
+    """qexpert_group with its scratch in the library's own fixed device array
+    (for callers that cannot allocate device memory)."""
+    f = lib().qexpert_group_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, P, P, P, P, P]
+    f.restype = I
+    _check(f(fmt, gs, _ptr(gate), _ptr(gate_s), _ptr(up), _ptr(up_s), _ptr(down), _ptr(down_s), E, D, F, _ptr(x),
+             s, k, _ptr(ids), _ptr(wts), _ptr(out), _ptr(status_dev), _stream(stream)))
