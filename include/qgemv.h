@@ -34,7 +34,7 @@
  *      QFMT_INT8_ROW   int8 codes [O][I], value = code; one scale per row
  *                      (gs must be 0 or I).
  *      QFMT_INT4_G     [O][I/2] bytes, the low nibble holds the even input i,
- *                      value = nibble - 8; gs a power of two >= 32.
+ *                      value = nibble - 8; gs a power of two in [32, 1024].
  *      QFMT_INT3_G64   plane A [O][I/4] (the low two bits of four codes per
  *                      byte, least significant first) followed in the same
  *                      buffer by plane B [O][I/8] (the high bit of eight codes
@@ -43,9 +43,11 @@
  *                      even input; gs must be 0 or 32.
  *  - Alignment: packed weights and activation/hidden vectors (x, h, workspace)
  *    16-byte aligned; scales and outputs 4-byte aligned; else QSTATUS_MISALIGNED.
- *  - Sizes: I % 16 == 0 (int8), I % gs == 0 (grouped formats), O, I, s >= 1;
- *    the activation rows of one launch are staged in shared memory, so
- *    I <= 51200 (else QSTATUS_BAD_DIM).
+ *  - Sizes: I % 16 == 0 (int8), I % gs == 0 (grouped formats), O, I, s >= 1.
+ *    The activation rows of one launch share shared memory with the weight
+ *    copy rings, so a row of I f32 must fit what the rings leave: I up to
+ *    about 27,000 (int8, int4, MXFP4) or 35,000 (int3); longer rows return
+ *    QSTATUS_BAD_DIM.
  */
 #ifndef QGEMV_GB300_H
 #define QGEMV_GB300_H

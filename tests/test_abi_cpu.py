@@ -59,6 +59,7 @@ A = 1 << 20
     (4, 64, 1056, -2),          # I not a multiple of gs
     (5, 0, 1000, -2),           # int3 I not a multiple of 64
     (4, 32, 51232, -2),         # row longer than the staging limit
+    (4, 2048, 4096, -1),        # int4 group above 1024
 ])
 def test_qgemv_rejects_bad_formats_and_sizes(L, fmt, gs, I, want):
     assert L.qgemv(fmt, gs, A, A, A, 16, I, 1, A, None) == want

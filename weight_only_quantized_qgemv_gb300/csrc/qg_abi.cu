@@ -45,7 +45,7 @@ static int check_fmt(int fmt, int gs, int I, int* gs_out)
         *gs_out = I;
         return QSTATUS_OK;
     case QFMT_INT4_G:
-        if (gs < 32 || (gs & (gs - 1))) return QSTATUS_BAD_FMT;
+        if (gs < 32 || gs > 1024 || (gs & (gs - 1))) return QSTATUS_BAD_FMT;
         if (I % gs) return QSTATUS_BAD_DIM;
         *gs_out = gs;
         return QSTATUS_OK;
@@ -64,12 +64,26 @@ static int check_fmt(int fmt, int gs, int I, int* gs_out)
     }
 }
 
-constexpr int kMaxI = 51200;   // one activation row of I f32 must fit the staging buffer
+constexpr int kMaxI = 51200;   // an upper bound; the shared-memory budget below decides
 
-static int rows_per_launch(int I)
+// Shared memory left for activation rows once the copy rings of a launch of
+// format fmt with nm matrices per row tile are placed.
+static size_t ring_bytes(int fmt, int nm)
 {
-    int s = kSmemMax / (I * (int)sizeof(float));
-    return s < kSmax ? s : kSmax;
+    switch (fmt) {
+    case QFMT_INT8_ROW: return ring_bytes_int8(nm);
+    case QFMT_INT4_G: return ring_bytes_int4(nm);
+    case QFMT_INT3_G64: return ring_bytes_int3(nm);
+    default: return ring_bytes_mxfp4(nm);
+    }
+}
+
+// Activation rows of length I one launch can stage (0: I is too long).
+static int rows_per_launch(int fmt, int nm, int I)
+{
+    const long long budget = (long long)kSmemMax - (long long)ring_bytes(fmt, nm) - 16;
+    long long s = budget > 0 ? budget / ((long long)I * (long long)sizeof(float)) : 0;
+    return (int)(s < kSmax ? s : kSmax);
 }
 
 #define QG_FMT_SWITCH(fmt, CALL)                                 \
@@ -210,7 +224,8 @@ int qgemv(int fmt, int gs, const void* w, const float* scales, const float* x, i
     const int grid = sm_count(&status);
     if (status) return status;
     const HostMat m{w, scales, O, I, g};
-    const int per = rows_per_launch(I);
+    const int per = rows_per_launch(fmt, 1, I);
+    if (per < 1) return QSTATUS_BAD_DIM;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     for (int s0 = 0; s0 < s; s0 += per) {
         const int n = s - s0 < per ? s - s0 : per;
@@ -240,7 +255,8 @@ int qgate_up(int fmt, int gs, const void* wg, const float* sg, const void* wu, c
     const int grid = sm_count(&status);
     if (status) return status;
     const HostMat mg{wg, sg, F, D, g}, mu{wu, su, F, D, g};
-    const int per = rows_per_launch(D);
+    const int per = rows_per_launch(fmt, 2, D);
+    if (per < 1) return QSTATUS_BAD_DIM;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     for (int s0 = 0; s0 < s; s0 += per) {
         const int n = s - s0 < per ? s - s0 : per;
@@ -291,8 +307,9 @@ int qexpert_group(int fmt, int gs, const void* gate, const float* gate_s, const 
     a.x = x; a.ids = ids; a.wts = wts; a.out = out;
     a.ws = static_cast<unsigned char*>(workspace);
     a.status_dev = status_dev;
-    const int big = D > F ? D : F;
-    a.smax = rows_per_launch(big);
+    const int up_rows = rows_per_launch(fmt, 2, D), down_rows = rows_per_launch(fmt, 1, F);
+    a.smax = up_rows < down_rows ? up_rows : down_rows;
+    if (a.smax < 1) return QSTATUS_BAD_DIM;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
     cudaError_t e = expert_prep(a, cs);

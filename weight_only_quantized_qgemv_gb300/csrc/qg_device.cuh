@@ -142,6 +142,23 @@ __device__ __forceinline__ void load_chunk(const Mat& m, long long o, int q, Chu
     }
 }
 
+// 128-bit load from shared memory at a 32-bit shared-window address.
+__device__ __forceinline__ float4 lds4s(uint32_t a)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+
+// (a & MASK) | c in one logic instruction.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+    return d;
+}
+
 // ---------------------------------------------------------------------------
 // Decoding.  A code c OR-ed into the mantissa of a float whose exponent is
 // chosen for the code's bit position gives 2^e + c exactly; subtracting
@@ -156,15 +173,23 @@ constexpr uint32_t kMag2 = 0x47000000u;   // 2^15, code at bits 8..
 constexpr uint32_t kMag3 = 0x45000000u;   // 2^11, code at bits 12..
 
 // int4 word (elements 8j..8j+7: low nibble first) -> four value pairs.
-__device__ __forceinline__ void decode_int4_word(uint32_t v, float2 (&d)[4])
+// mg[k] holds the exponent for nibble position k of a 16-bit half.
+struct Int4Magic {
+    uint32_t m0, m1, m2, m3;
+    float2 b01, b23;
+    __device__ __forceinline__ Int4Magic()
+        : m0(kMag0), m1(kMag1), m2(kMag2), m3(kMag3),
+          b01(make_float2(-8388616.0f, -524296.0f)),   // -(2^23 + 8), -(2^19 + 8)
+          b23(make_float2(-32776.0f, -2056.0f)) {}     // -(2^15 + 8), -(2^11 + 8)
+};
+
+__device__ __forceinline__ void decode_int4_word(uint32_t v, const Int4Magic& g, float2 (&d)[4])
 {
-    const float2 B01 = make_float2(-8388616.0f, -524296.0f);   // -(2^23 + 8), -(2^19 + 8)
-    const float2 B23 = make_float2(-32776.0f, -2056.0f);       // -(2^15 + 8), -(2^11 + 8)
     const uint32_t h = v >> 16;
-    d[0] = fadd2(make_float2(u2f((v & 0x000Fu) | kMag0), u2f((v & 0x00F0u) | kMag1)), B01);
-    d[1] = fadd2(make_float2(u2f((v & 0x0F00u) | kMag2), u2f((v & 0xF000u) | kMag3)), B23);
-    d[2] = fadd2(make_float2(u2f((h & 0x000Fu) | kMag0), u2f((h & 0x00F0u) | kMag1)), B01);
-    d[3] = fadd2(make_float2(u2f((h & 0x0F00u) | kMag2), u2f((h & 0xF000u) | kMag3)), B23);
+    d[0] = fadd2(make_float2(u2f(and_or<0x000Fu>(v, g.m0)), u2f(and_or<0x00F0u>(v, g.m1))), g.b01);
+    d[1] = fadd2(make_float2(u2f(and_or<0x0F00u>(v, g.m2)), u2f(and_or<0xF000u>(v, g.m3))), g.b23);
+    d[2] = fadd2(make_float2(u2f(and_or<0x000Fu>(h, g.m0)), u2f(and_or<0x00F0u>(h, g.m1))), g.b01);
+    d[3] = fadd2(make_float2(u2f(and_or<0x0F00u>(h, g.m2)), u2f(and_or<0xF000u>(h, g.m3))), g.b23);
 }
 
 // int8 word (elements 4j..4j+3) -> two value pairs.  b ^ 0x80 = b + 128.
@@ -227,17 +252,18 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int j)
     return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
 // ---------------------------------------------------------------------------
 // Chunk consumption: for NR chunk rows (one chunk each) and S activation rows,
-// acc[rr][s] += scale[rr] * sum_chunk value(code) * x_s.  Word-major order
-// keeps only one word's decoded values and one x quad pair live at a time.
-// xb[s] points at the chunk's swizzled x segment; xo[j] = 4 * (j ^ swz).
+// acc[rr][s] += scale[rr] * sum_chunk value(code) * x_s.
+// xq[s] is the shared-memory address of the chunk's swizzled x segment of
+// activation row s; xo[j] = 16 * (j ^ swz) is this lane's byte offset of quad j.
+// With one activation row, decoding and multiplying go row by row, the x quads
+// of a word shared by all NR rows; with several, a word is decoded once for
+// all of them.
 // ---------------------------------------------------------------------------
 template <int FMT, int S, int NR>
 __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (&sc)[NR],
-                                        const float* const (&xb)[S], const int (&xo)[8], float (&acc)[NR][S])
+                                        const uint32_t (&xq)[S], const uint32_t (&xo)[8], float (&acc)[NR][S])
 {
     float2 part[NR][S];
 #pragma unroll
@@ -246,24 +272,40 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
         for (int s = 0; s < S; s++) part[rr][s] = make_float2(0.f, 0.f);
 
     if constexpr (FMT == FMT_INT4_G || FMT == FMT_MXFP4_G32) {
+        [[maybe_unused]] const Int4Magic g;
 #pragma unroll
         for (int j = 0; j < 4; j++) {
-            float2 d[NR][4];
-#pragma unroll
-            for (int rr = 0; rr < NR; rr++) {
-                if constexpr (FMT == FMT_INT4_G) decode_int4_word(word(c[rr].w, j), d[rr]);
-                else decode_mxfp4_word(word(c[rr].w, j), d[rr]);
-            }
-#pragma unroll
-            for (int s = 0; s < S; s++) {
-                const float4 xa = lds4(xb[s] + xo[2 * j]);
-                const float4 xc = lds4(xb[s] + xo[2 * j + 1]);
+            if constexpr (S == 1) {
+                const float4 xa = lds4s(xq[0] + xo[2 * j]);
+                const float4 xc = lds4s(xq[0] + xo[2 * j + 1]);
 #pragma unroll
                 for (int rr = 0; rr < NR; rr++) {
-                    part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
-                    part[rr][s] = ffma2(d[rr][1], make_float2(xa.z, xa.w), part[rr][s]);
-                    part[rr][s] = ffma2(d[rr][2], make_float2(xc.x, xc.y), part[rr][s]);
-                    part[rr][s] = ffma2(d[rr][3], make_float2(xc.z, xc.w), part[rr][s]);
+                    float2 d[4];
+                    if constexpr (FMT == FMT_INT4_G) decode_int4_word(word(c[rr].w, j), g, d);
+                    else decode_mxfp4_word(word(c[rr].w, j), d);
+                    part[rr][0] = ffma2(d[0], make_float2(xa.x, xa.y), part[rr][0]);
+                    part[rr][0] = ffma2(d[1], make_float2(xa.z, xa.w), part[rr][0]);
+                    part[rr][0] = ffma2(d[2], make_float2(xc.x, xc.y), part[rr][0]);
+                    part[rr][0] = ffma2(d[3], make_float2(xc.z, xc.w), part[rr][0]);
+                }
+            } else {
+                float2 d[NR][4];
+#pragma unroll
+                for (int rr = 0; rr < NR; rr++) {
+                    if constexpr (FMT == FMT_INT4_G) decode_int4_word(word(c[rr].w, j), g, d[rr]);
+                    else decode_mxfp4_word(word(c[rr].w, j), d[rr]);
+                }
+#pragma unroll
+                for (int s = 0; s < S; s++) {
+                    const float4 xa = lds4s(xq[s] + xo[2 * j]);
+                    const float4 xc = lds4s(xq[s] + xo[2 * j + 1]);
+#pragma unroll
+                    for (int rr = 0; rr < NR; rr++) {
+                        part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
+                        part[rr][s] = ffma2(d[rr][1], make_float2(xa.z, xa.w), part[rr][s]);
+                        part[rr][s] = ffma2(d[rr][2], make_float2(xc.x, xc.y), part[rr][s]);
+                        part[rr][s] = ffma2(d[rr][3], make_float2(xc.z, xc.w), part[rr][s]);
+                    }
                 }
             }
         }
@@ -275,7 +317,7 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
             for (int rr = 0; rr < NR; rr++) decode_int8_word(word(c[rr].w, j), d[rr]);
 #pragma unroll
             for (int s = 0; s < S; s++) {
-                const float4 xa = lds4(xb[s] + xo[j]);
+                const float4 xa = lds4s(xq[s] + xo[j]);
 #pragma unroll
                 for (int rr = 0; rr < NR; rr++) {
                     part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
@@ -300,11 +342,11 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
                 const int qd = 4 * j + m;
 #pragma unroll
                 for (int s = 0; s < S; s++) {
-                    const float4 xq = lds4(xb[s] + (qd >= 8 ? 32 : 0) + xo[qd & 7]);
+                    const float4 xv = lds4s(xq[s] + (qd >= 8 ? 128u : 0u) + xo[qd & 7]);
 #pragma unroll
                     for (int rr = 0; rr < NR; rr++) {
-                        part[rr][s] = ffma2(d[rr][0], make_float2(xq.x, xq.y), part[rr][s]);
-                        part[rr][s] = ffma2(d[rr][1], make_float2(xq.z, xq.w), part[rr][s]);
+                        part[rr][s] = ffma2(d[rr][0], make_float2(xv.x, xv.y), part[rr][s]);
+                        part[rr][s] = ffma2(d[rr][1], make_float2(xv.z, xv.w), part[rr][s]);
                     }
                 }
             }
@@ -373,47 +415,141 @@ __device__ __forceinline__ int reduce_scatter_index(int lane)
 __host__ __device__ constexpr int pow2_ceil(int v) { int p = 1; while (p < v) p <<= 1; return p; }
 
 // ---------------------------------------------------------------------------
+// Asynchronous copies of 16, 8 and 4 bytes global -> shared (L2 only for the
+// 16-byte weight chunks).  Each lane copies, and later reads back, only its
+// own chunks, so completion is per thread (cp.async groups) and no barrier or
+// spin-wait is involved.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+__device__ __forceinline__ uint4 lds16(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds8(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+
+// Bytes of one ring slot: NR chunk rows x 32 lanes (16 B of codes, int3 also
+// 8 B of plane B) and their scales.
+template <int FMT, int NR>
+__host__ __device__ constexpr int ring_slot_bytes()
+{
+    return NR * 32 * (16 + (FMT == FMT_INT3_G64 ? 8 : 0) + 4);
+}
+
+// ---------------------------------------------------------------------------
 // Row streaming.  A warp processes row tiles of R rows (of NM matrices sharing
-// the same row index: NM = 2 for gate and up).  Tiles tile_first,
+// the same row index: NM = 2 for gate and up): tiles tile_first,
 // tile_first + tile_step, ... below ntiles, rows row0 + tile * R + r < row_end.
-// Work is the flattened sequence (tile, step); step c covers chunk c*32 + lane.
-// The sink is called once per finished tile from every lane:
-//   sink(lane_idx_value, value_index, valid_lane) where value index
-//   v = (s * R + r) * NM + m.
+// Work is the flattened sequence (tile, step); step c covers chunk c*32 + lane
+// of each row.  Copies run P steps ahead of use through a ring of P slots in
+// this warp's part of shared memory.  Each row's chunk and scale addresses are
+// set once per tile and advance by a constant per step.  The sink is called
+// once per finished tile from every lane: sink(value, index, lane_holds_it,
+// first row of the tile, row_end) with index v = (s * R + r) * NM + m.
 // ---------------------------------------------------------------------------
 template <int FMT, int S, int R, int P, int NM>
 struct RowStreamer {
     static constexpr int EPL = Traits<FMT>::EPL;
+    static constexpr int NR = NM * R;
     static constexpr int V = pow2_ceil(S * R * NM);
+    static constexpr int SLOT = ring_slot_bytes<FMT, NR>();
+    static constexpr int B_OFF = NR * 32 * 16;                                  // plane B part of a slot
+    static constexpr int S_OFF = NR * 32 * (16 + (FMT == FMT_INT3_G64 ? 8 : 0)); // scales part of a slot
 
-    Chunk<FMT> slot[P][NM * R];
-    float ssc[P][NM * R];
-    int it_tile, it_c;      // issue pointer
-    int ct_tile, ct_c;      // consume pointer
-    int total, done;
+    const uint8_t* wp[NR];    // this lane's next chunk of each row (int3: plane A)
+    const uint8_t* bp[NR];    // int3 plane B
+    const float* sp[NR];      // this lane's next scale of each row
+    int sstep;                // scale advance per step
+    uint32_t ring;            // this lane's byte position in slot 0 of the warp's ring
 
     Mat mats[NM];
     long long row0, row_end;
-    int nchunks, nsteps, tile_step, lane;
+    int it_tile, it_c, ct_tile, ct_c;
+    int total, issued, nchunks, nsteps, ntiles, tile_step, lane;
 
-    __device__ __forceinline__ void issue(int p)
+    __device__ __forceinline__ void set_tile(int tile)
     {
-        const int q = it_c * 32 + lane;
-        const bool ok = q < nchunks;
 #pragma unroll
         for (int r = 0; r < R; r++) {
-            long long o = row0 + (long long)it_tile * R + r;
+            long long o = row0 + (long long)tile * R + r;
             o = o < row_end ? o : row_end - 1;       // tail rows: load a valid row, drop the result
 #pragma unroll
             for (int m = 0; m < NM; m++) {
-                if (ok) load_chunk<FMT>(mats[m], o, q, slot[p][m * R + r], ssc[p][m * R + r]);
+                const Mat& M = mats[m];
+                const int rr = m * R + r;
+                if constexpr (FMT == FMT_INT8_ROW) {
+                    wp[rr] = M.w + o * M.I + lane * 16;
+                    sp[rr] = M.sc + o;
+                } else if constexpr (FMT == FMT_INT3_G64) {
+                    wp[rr] = M.w + o * (long long)(M.I / 4) + lane * 16;
+                    bp[rr] = M.w + M.O * (long long)(M.I / 4) + o * (long long)(M.I / 8) + lane * 8;
+                    sp[rr] = M.sc + o * M.ngrp + lane;
+                } else {
+                    wp[rr] = M.w + o * (long long)(M.I / 2) + lane * 16;
+                    sp[rr] = M.sc + o * M.ngrp + (lane >> M.gsh);
+                }
             }
         }
-        if (++it_c == nsteps) { it_c = 0; it_tile += tile_step; }
     }
 
+    // Copies of the next step into slot p; one cp.async group per call, empty
+    // past the end, so group counts stay aligned with steps.
+    __device__ __forceinline__ void issue(int p)
+    {
+        if (issued < total) {
+            const bool ok = it_c * 32 + lane < nchunks;
+            const uint32_t slot = ring + (uint32_t)(p * SLOT);
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) {
+                if (ok) {
+                    cp_async16(slot + rr * 512, wp[rr]);
+                    if constexpr (FMT == FMT_INT3_G64) cp_async8(slot + B_OFF + rr * 256 - lane * 8, bp[rr]);
+                    cp_async4(slot + S_OFF + rr * 128 - lane * 12, sp[rr]);
+                }
+                wp[rr] += 512;
+                if constexpr (FMT == FMT_INT3_G64) bp[rr] += 256;
+                sp[rr] += sstep;
+            }
+            ++issued;
+            if (++it_c == nsteps) {
+                it_c = 0;
+                it_tile += tile_step;
+                if (it_tile < ntiles) set_tile(it_tile);
+            }
+        }
+        cp_async_commit();
+    }
+
+    // ring_warp: shared address of this warp's ring (P slots of SLOT bytes).
     __device__ __forceinline__ void begin(const Mat* m, long long row0_, long long row_end_, int tile_first,
-                                          int ntiles, int tile_step_, int lane_)
+                                          int ntiles_, int tile_step_, int lane_, uint32_t ring_warp)
     {
 #pragma unroll
         for (int k = 0; k < NM; k++) mats[k] = m[k];
@@ -421,30 +557,37 @@ struct RowStreamer {
         row_end = row_end_;
         lane = lane_;
         tile_step = tile_step_;
+        ntiles = ntiles_;
+        ring = ring_warp + (uint32_t)lane * 16;
         nchunks = m[0].I / EPL;
         nsteps = (nchunks + 31) / 32;
+        // int8: one scale per row; int4: 32 chunks span 32 >> gsh groups
+        sstep = FMT == FMT_INT8_ROW ? 0 : (32 >> m[0].gsh);
         const int my_tiles = tile_first < ntiles ? (ntiles - tile_first + tile_step - 1) / tile_step : 0;
         total = my_tiles * nsteps;
+        issued = 0;
         it_tile = ct_tile = tile_first;
         it_c = ct_c = 0;
-        done = 0;
+        if (total > 0) set_tile(it_tile);
 #pragma unroll
-        for (int p = 0; p < P; p++)
-            if (p < total) issue(p);
+        for (int p = 0; p < P; p++) issue(p);
     }
 
-    // xbase[s]: swizzled x rows (token slots) in shared memory.
+    // xs[s]: shared-memory addresses of the swizzled activation rows.
     template <class Sink>
-    __device__ __forceinline__ void run(const float* const (&xbase)[S], Sink& sink)
+    __device__ __forceinline__ void run(const uint32_t (&xs)[S], Sink& sink)
     {
-        const int swz = x_swz(EPL, lane);
-        int xo[8];
+        const uint32_t swz = (uint32_t)x_swz(EPL, lane);
+        uint32_t xo[8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) xo[j] = 4 * (j ^ swz);
+        for (int j = 0; j < 8; j++) xo[j] = 16u * ((uint32_t)j ^ swz);
+        uint32_t xl[S];                      // this lane's first chunk segment of each row
+#pragma unroll
+        for (int s = 0; s < S; s++) xl[s] = xs[s] + (uint32_t)lane * (EPL * 4);
 
-        float acc[NM * R][S];
+        float acc[NR][S];
 #pragma unroll
-        for (int rr = 0; rr < NM * R; rr++)
+        for (int rr = 0; rr < NR; rr++)
 #pragma unroll
             for (int s = 0; s < S; s++) acc[rr][s] = 0.f;
 
@@ -452,14 +595,27 @@ struct RowStreamer {
 #pragma unroll
             for (int p = 0; p < P; p++) {
                 if (j0 + p < total) {
-                    const int q = ct_c * 32 + lane;
-                    if (q < nchunks) {
-                        const float* xb[S];
+                    cp_async_wait<P - 1>();          // this step's copies have landed
+                    if (ct_c * 32 + lane < nchunks) {
+                        const uint32_t slot = ring + (uint32_t)(p * SLOT);
+                        Chunk<FMT> c[NR];
+                        float sc[NR];
 #pragma unroll
-                        for (int s = 0; s < S; s++) xb[s] = xbase[s] + q * EPL;
-                        consume<FMT, S, NM * R>(slot[p], ssc[p], xb, xo, acc);
+                        for (int rr = 0; rr < NR; rr++) {
+                            if constexpr (FMT == FMT_INT3_G64) {
+                                c[rr].a = lds16(slot + rr * 512);
+                                c[rr].b = lds8(slot + B_OFF + rr * 256 - lane * 8);
+                            } else {
+                                c[rr].w = lds16(slot + rr * 512);
+                            }
+                            sc[rr] = lds_f32(slot + S_OFF + rr * 128 - lane * 12);
+                        }
+                        uint32_t xq[S];
+#pragma unroll
+                        for (int s = 0; s < S; s++) xq[s] = xl[s] + (uint32_t)ct_c * (32 * EPL * 4);
+                        consume<FMT, S, NR>(c, sc, xq, xo, acc);
                     }
-                    if (j0 + p + P < total) issue(p);
+                    issue(p);
                     if (++ct_c == nsteps) {
                         // finished tile ct_tile: reduce and hand to the sink
                         float v[V];
@@ -483,6 +639,7 @@ struct RowStreamer {
                 }
             }
         }
+        cp_async_wait<0>();
     }
 };
 

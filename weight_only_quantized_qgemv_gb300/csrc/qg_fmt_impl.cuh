@@ -26,15 +26,23 @@ constexpr int EPL = Traits<FMT>::EPL;
 // accumulators (S x NM x R) so everything stays in registers.
 // int3 chunks take 7 registers instead of 5, so their budget is 4
 // accumulators beyond the single-row-set case.
+#ifndef QG_RMAX
+#define QG_RMAX 4
+#endif
 template <int S, int NM>
 __host__ __device__ constexpr int rows_per_tile()
 {
-    constexpr int acc_budget = (FMT == FMT_INT3_G64 && S * NM > 1) ? 4 : 8;
+    constexpr int acc_budget = FMT == FMT_INT3_G64 ? 4 : 8;
+    constexpr int rmax = FMT == FMT_INT3_G64 ? 2 : QG_RMAX;
     constexpr int by_acc = acc_budget / (S * NM) > 0 ? acc_budget / (S * NM) : 1;
-    return (4 / NM) < by_acc ? (4 / NM) : by_acc;
+    constexpr int by_rows = rmax / NM > 0 ? rmax / NM : 1;
+    return by_rows < by_acc ? by_rows : by_acc;
 }
 
-constexpr int kRing = 2;   // chunk-register ring depth
+#ifndef QG_RING
+#define QG_RING 3
+#endif
+constexpr int kRing = QG_RING;   // chunk-register ring depth
 
 inline Mat to_mat(const HostMat& h)
 {
@@ -55,8 +63,23 @@ inline Mat to_mat(const HostMat& h)
 // ---------------------------------------------------------------------------
 
 // One matrix (or a gate/up pair) against s <= 8 activation rows.
+// Shared-memory layout of every streaming launch: the activation rows at
+// offset 0, then one cp.async ring per warp at ring_off + warp * ring_stride.
+struct RingLayout {
+    int ring_off;
+    int ring_stride;
+};
+
+// Ring bytes per warp: kRing slots sized for the largest tile of the family
+// (one activation row).
 template <int NM>
-struct DenseJob {
+__host__ __device__ constexpr int ring_stride_bytes()
+{
+    return kRing * ring_slot_bytes<FMT, NM * rows_per_tile<1, NM>()>();
+}
+
+template <int NM>
+struct DenseJob : RingLayout {
     Mat m[NM];
     const float* x;      // [S][I]
     float* y;            // y[s * ldy + row]
@@ -78,7 +101,7 @@ struct DenseJob {
 
 // Expert phase A: the gate and up rows of every used expert, against the
 // tokens routed to it; stores h = silu(g) * u per sorted pair.
-struct ExpertUpJob {
+struct ExpertUpJob : RingLayout {
     Mat gate0, up0;                 // expert 0's matrices (w, sc advanced per expert)
     long long mat_bytes, mat_scales;
     const float* x;
@@ -111,7 +134,7 @@ struct ExpertUpJob {
 
 // Expert phase B: the down rows of every used expert against the h vectors of
 // its pairs; stores z = down h per sorted pair.
-struct ExpertDownJob {
+struct ExpertDownJob : RingLayout {
     Mat down0;
     long long mat_bytes, mat_scales;
     const int32_t* hdr;
@@ -175,7 +198,9 @@ __device__ __noinline__ void segment(const Job job, int b, long long l0, long lo
     job.mats(b, m);
     const int ntiles = (int)((l1 - l0 + R - 1) / R);
     RowStreamer<FMT, S, R, kRing, NM> st;
-    st.begin(m, l0, l1, warp, ntiles, kWarps, lane);      // weight loads in flight during staging
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(xs);
+    st.begin(m, l0, l1, warp, ntiles, kWarps, lane,
+             base + (uint32_t)(job.ring_off + warp * job.ring_stride));   // copies in flight during staging
     const int I = m[0].I;
     if (b != staged) {
         __syncthreads();
@@ -186,11 +211,11 @@ __device__ __noinline__ void segment(const Job job, int b, long long l0, long lo
         __syncthreads();
         staged = b;
     }
-    const float* xb[S];
+    uint32_t xsh[S];
 #pragma unroll
-    for (int s = 0; s < S; s++) xb[s] = xs + (long long)s * I;
+    for (int s = 0; s < S; s++) xsh[s] = base + (uint32_t)(s * I) * 4u;
     Sink<Job, S, R, NM> sink{job, b};
-    st.run(xb, sink);
+    st.run(xsh, sink);
 }
 
 template <int NM, int S, int SMAX, class Job>
@@ -241,7 +266,7 @@ __device__ __forceinline__ void decode_chunk(const Chunk<F_>& c, float* v)
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             float2 d[4];
-            if constexpr (F_ == FMT_INT4_G) decode_int4_word(word(c.w, j), d);
+            if constexpr (F_ == FMT_INT4_G) decode_int4_word(word(c.w, j), Int4Magic(), d);
             else decode_mxfp4_word(word(c.w, j), d);
 #pragma unroll
             for (int k = 0; k < 4; k++) {
@@ -357,7 +382,9 @@ cudaError_t QG_CAT(gemv_, QG_NAME)(const HostMat& hm, const float* x, int s, flo
     job.y = y;
     job.ldy = ldy;
     job.S = s;
-    return launch_dense_s<1>(job, s, grid, (size_t)s * hm.I * sizeof(float), st);
+    job.ring_off = (int)align16((size_t)s * hm.I * sizeof(float));
+    job.ring_stride = ring_stride_bytes<1>();
+    return launch_dense_s<1>(job, s, grid, job.ring_off + (size_t)kWarps * job.ring_stride, st);
 }
 
 cudaError_t QG_CAT(gate_up_, QG_NAME)(const HostMat& g, const HostMat& u, const float* x, int s, float* h,
@@ -370,7 +397,9 @@ cudaError_t QG_CAT(gate_up_, QG_NAME)(const HostMat& g, const HostMat& u, const 
     job.y = h;
     job.ldy = ldh;
     job.S = s;
-    return launch_dense_s<2>(job, s, grid, (size_t)s * g.I * sizeof(float), st);
+    job.ring_off = (int)align16((size_t)s * g.I * sizeof(float));
+    job.ring_stride = ring_stride_bytes<2>();
+    return launch_dense_s<2>(job, s, grid, job.ring_off + (size_t)kWarps * job.ring_stride, st);
 }
 
 cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st)
@@ -391,8 +420,10 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
     job.h = reinterpret_cast<float*>(a.ws + L.h);
     job.D = a.D;
     job.F = a.F;
+    job.ring_off = (int)align16((size_t)a.smax * a.D * sizeof(float));
+    job.ring_stride = ring_stride_bytes<2>();
     auto kern = k_stream<2, 1, kSmax, ExpertUpJob>;
-    const size_t smem = (size_t)a.smax * a.D * sizeof(float);
+    const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
     static int granted[64];
     cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
@@ -416,13 +447,20 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
     job.z = reinterpret_cast<float*>(a.ws + L.z);
     job.D = a.D;
     job.F = a.F;
+    job.ring_off = (int)align16((size_t)a.smax * a.F * sizeof(float));
+    job.ring_stride = ring_stride_bytes<1>();
     auto kern = k_stream<1, 1, kSmax, ExpertDownJob>;
-    const size_t smem = (size_t)a.smax * a.F * sizeof(float);
+    const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
     static int granted[64];
     cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(job);
     return cudaGetLastError();
+}
+
+size_t QG_CAT(ring_bytes_, QG_NAME)(int nm)
+{
+    return (size_t)kWarps * (nm == 2 ? ring_stride_bytes<2>() : ring_stride_bytes<1>());
 }
 
 cudaError_t QG_CAT(dequant_, QG_NAME)(const HostMat& hm, float* out, cudaStream_t st)

@@ -6,11 +6,14 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/qgemv.h"
+#include "qgemv.h"
 
 namespace qg {
 
-constexpr int kWarps = 16;                  // warps per CTA of the streaming kernels
+#ifndef QG_WARPS
+#define QG_WARPS 16
+#endif
+constexpr int kWarps = QG_WARPS;            // warps per CTA of the streaming kernels
 constexpr int kThreads = kWarps * 32;
 constexpr int kSmax = 8;                    // activation rows per launch / per expert batch
 constexpr int kSmemMax = 227 * 1024;        // dynamic shared memory per CTA (sm_103a)
@@ -37,6 +40,7 @@ struct WsLayout {
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
 inline WsLayout ws_layout(int D, int F, int s, int k)
 {
@@ -76,7 +80,8 @@ struct ExpertArgs {
                                long long ldh, int grid, cudaStream_t st);                              \
     cudaError_t expert_up_##name(const ExpertArgs& a, int grid, cudaStream_t st);                       \
     cudaError_t expert_down_##name(const ExpertArgs& a, int grid, cudaStream_t st);                     \
-    cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);
+    cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);                         \
+    size_t ring_bytes_##name(int nm);
 
 QG_DECLARE_FMT(int8)
 QG_DECLARE_FMT(int4)
