@@ -176,6 +176,15 @@ const char* qstatus_string(int status);
 /* Text of the CUDA error behind the calling thread's last QSTATUS_LAUNCH. */
 const char* qlast_cuda_error(void);
 
+/*
+ * QSTATUS_DEVICE_TIMEOUT when a bounded device-side wait in one of this
+ * library's kernels ran out on the current device since the last clear (the
+ * results of that launch are undefined; qexpert_group also reports it in its
+ * status word), else QSTATUS_OK.  Reads a device word, so it synchronizes with
+ * the device; clear != 0 resets the word.
+ */
+int qdevice_error(int clear);
+
 #ifdef __cplusplus
 }
 #endif

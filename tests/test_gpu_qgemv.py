@@ -104,3 +104,16 @@ def test_qgemv_full_size_repeatable():
     a = run_gemv(wl.fmt, wl.gs, w, sc, x, wl.O, wl.I)
     b = run_gemv(wl.fmt, wl.gs, w, sc, x, wl.O, wl.I)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fmt,gs,I", [(INT8_ROW, 0, 1040), (INT4_G, 32, 2080), (INT3_G64, 0, 2112),
+                                      (MXFP4_G32, 0, 2080)])
+def test_qgemv_row_bits_do_not_depend_on_batch(fmt, gs, I):
+    """An activation row gets the same bits alone as in a batch of 5 (colibri's
+    expert tier states the same of its per-row GEMV)."""
+    O, s = 130, 5
+    g, w, sc, x = inputs(fmt, gs, O, I, s, 29)
+    ys = run_gemv(fmt, gs, w, sc, x, O, I)
+    for t in range(s):
+        y1 = run_gemv(fmt, gs, w, sc, x[t:t + 1], O, I)
+        assert np.array_equal(y1[0], ys[t])

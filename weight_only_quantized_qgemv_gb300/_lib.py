@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.qstatus_string.restype = ctypes.c_char_p
         L.qlast_cuda_error.argtypes = []
         L.qlast_cuda_error.restype = ctypes.c_char_p
+        L.qdevice_error.argtypes = [I]
+        L.qdevice_error.restype = I
         _lib = L
     return _lib
 
@@ -97,6 +99,12 @@ def _check(status: int):
 
 def qstatus_string(status: int) -> str:
     return lib().qstatus_string(status).decode()
+
+
+def qdevice_error(clear: bool = False) -> int:
+    """QSTATUS_DEVICE_TIMEOUT if a bounded device-side wait ran out since the
+    last clear, else QSTATUS_OK (synchronizes with the device)."""
+    return lib().qdevice_error(1 if clear else 0)
 
 
 def qgemv(fmt, gs, w, scales, x, O, I, s, y, stream=None):

@@ -211,6 +211,15 @@ const char* qstatus_string(int status)
 
 const char* qlast_cuda_error(void) { return g_last_cuda_error; }
 
+int qdevice_error(int clear)
+{
+    const int e[4] = {device_error_int8(clear), device_error_int4(clear), device_error_int3(clear),
+                      device_error_mxfp4(clear)};
+    for (int v : e)
+        if (v != QSTATUS_OK) return v;
+    return QSTATUS_OK;
+}
+
 int qgemv(int fmt, int gs, const void* w, const float* scales, const float* x, int O, int I, int s, float* y,
           void* stream)
 {
@@ -309,6 +318,8 @@ int qexpert_group(int fmt, int gs, const void* gate, const float* gate_s, const 
     a.status_dev = status_dev;
     const int up_rows = rows_per_launch(fmt, 2, D), down_rows = rows_per_launch(fmt, 1, F);
     a.smax = up_rows < down_rows ? up_rows : down_rows;
+    if (a.smax > kExpertSmax) a.smax = kExpertSmax;
+    if (a.smax > s) a.smax = s;   // a batch holds pairs of distinct tokens unless a token repeats an id
     if (a.smax < 1) return QSTATUS_BAD_DIM;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 

@@ -142,12 +142,28 @@ __device__ __forceinline__ void load_chunk(const Mat& m, long long o, int q, Chu
     }
 }
 
-// 128-bit load from shared memory at a 32-bit shared-window address.
+#ifndef QG_CXX_LDS
+#define QG_CXX_LDS 1
+#endif
+
+// The kernels' dynamic shared memory; every shared address below is a byte
+// offset from its start.
+extern __shared__ float4 qg_smem4[];
+
+__device__ __forceinline__ uint32_t smem_base() { return (uint32_t)__cvta_generic_to_shared(qg_smem4); }
+
+// Loads from shared memory at byte offset a.  Plain loads let the compiler
+// schedule them; the cp.async waits (memory clobbers) still order them.
 __device__ __forceinline__ float4 lds4s(uint32_t a)
 {
+#if QG_CXX_LDS
+    return *reinterpret_cast<const float4*>(reinterpret_cast<const char*>(qg_smem4) + a);
+#else
     float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a + smem_base()));
     return v;
+#endif
 }
 
 // (a & MASK) | c in one logic instruction.
@@ -263,8 +279,11 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int j)
 // ---------------------------------------------------------------------------
 template <int FMT, int S, int NR>
 __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (&sc)[NR],
-                                        const uint32_t (&xq)[S], const uint32_t (&xo)[8], float (&acc)[NR][S])
+                                        const uint32_t (&xq)[S], const uint32_t (&xo)[8], float (&acc)[S][NR],
+                                        int s_act)
 {
+    // Every (row, activation row) accumulates in the same order whatever S is,
+    // so a row's bits do not depend on how many activation rows share its launch.
     float2 part[NR][S];
 #pragma unroll
     for (int rr = 0; rr < NR; rr++)
@@ -297,11 +316,12 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
                 }
 #pragma unroll
                 for (int s = 0; s < S; s++) {
+                    if (s >= s_act) break;                       // warp-uniform: activation rows in use
                     const float4 xa = lds4s(xq[s] + xo[2 * j]);
                     const float4 xc = lds4s(xq[s] + xo[2 * j + 1]);
 #pragma unroll
                     for (int rr = 0; rr < NR; rr++) {
-                        part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
+                            part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
                         part[rr][s] = ffma2(d[rr][1], make_float2(xa.z, xa.w), part[rr][s]);
                         part[rr][s] = ffma2(d[rr][2], make_float2(xc.x, xc.y), part[rr][s]);
                         part[rr][s] = ffma2(d[rr][3], make_float2(xc.z, xc.w), part[rr][s]);
@@ -314,9 +334,12 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
         for (int j = 0; j < 4; j++) {
             float2 d[NR][2];
 #pragma unroll
-            for (int rr = 0; rr < NR; rr++) decode_int8_word(word(c[rr].w, j), d[rr]);
+            for (int rr = 0; rr < NR; rr++) {
+                decode_int8_word(word(c[rr].w, j), d[rr]);
+            }
 #pragma unroll
             for (int s = 0; s < S; s++) {
+                if (s >= s_act) break;
                 const float4 xa = lds4s(xq[s] + xo[j]);
 #pragma unroll
                 for (int rr = 0; rr < NR; rr++) {
@@ -338,14 +361,17 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
             for (int m = 0; m < 4; m++) {
                 float2 d[NR][2];
 #pragma unroll
-                for (int rr = 0; rr < NR; rr++) decode_int3_quad(cls[rr], m, d[rr]);
+                for (int rr = 0; rr < NR; rr++) {
+                    decode_int3_quad(cls[rr], m, d[rr]);
+                }
                 const int qd = 4 * j + m;
 #pragma unroll
                 for (int s = 0; s < S; s++) {
+                    if (s >= s_act) break;
                     const float4 xv = lds4s(xq[s] + (qd >= 8 ? 128u : 0u) + xo[qd & 7]);
 #pragma unroll
                     for (int rr = 0; rr < NR; rr++) {
-                        part[rr][s] = ffma2(d[rr][0], make_float2(xv.x, xv.y), part[rr][s]);
+                            part[rr][s] = ffma2(d[rr][0], make_float2(xv.x, xv.y), part[rr][s]);
                         part[rr][s] = ffma2(d[rr][1], make_float2(xv.z, xv.w), part[rr][s]);
                     }
                 }
@@ -355,7 +381,7 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
 #pragma unroll
     for (int rr = 0; rr < NR; rr++)
 #pragma unroll
-        for (int s = 0; s < S; s++) acc[rr][s] = fmaf(part[rr][s].x + part[rr][s].y, sc[rr], acc[rr][s]);
+        for (int s = 0; s < S; s++) acc[s][rr] = fmaf(part[rr][s].x + part[rr][s].y, sc[rr], acc[s][rr]);
 }
 
 // ---------------------------------------------------------------------------
@@ -375,6 +401,20 @@ __device__ __forceinline__ void stage_rows(float* xs, int xstride, const float* 
 }
 
 __host__ __device__ constexpr int ilog2(int v) { int l = 0; while ((1 << l) < v) l++; return l; }
+
+// The same staging done by threads [0, nthreads) only (t = this thread).
+template <int EPL>
+__device__ __forceinline__ void stage_rows_part(float* xs, int xstride, const float* const* src, int nrows, int I,
+                                                int t, int nthreads)
+{
+    const int nq = I / 4;
+    for (int idx = t; idx < nrows * nq; idx += nthreads) {
+        const int s = idx / nq;
+        const int qd = idx - s * nq;
+        const float4 v = *reinterpret_cast<const float4*>(src[s] + 4 * qd);
+        *reinterpret_cast<float4*>(xs + (long long)s * xstride + 4 * x_quad_phys(EPL, qd)) = v;
+    }
+}
 
 // ---------------------------------------------------------------------------
 // Transposed warp reduction of V (power of two, <= 32) values: afterwards lane
@@ -420,6 +460,7 @@ __host__ __device__ constexpr int pow2_ceil(int v) { int p = 1; while (p < v) p 
 // own chunks, so completion is per thread (cp.async groups) and no barrier or
 // spin-wait is involved.
 // ---------------------------------------------------------------------------
+// dst: absolute shared-window address.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
@@ -438,21 +479,89 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 __device__ __forceinline__ uint4 lds16(uint32_t a)
 {
+#if QG_CXX_LDS
+    return *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(qg_smem4) + a);
+#else
     uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a + smem_base()));
     return v;
+#endif
 }
 __device__ __forceinline__ uint2 lds8(uint32_t a)
 {
+#if QG_CXX_LDS
+    return *reinterpret_cast<const uint2*>(reinterpret_cast<const char*>(qg_smem4) + a);
+#else
     uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a + smem_base()));
     return v;
+#endif
 }
 __device__ __forceinline__ float lds_f32(uint32_t a)
 {
+#if QG_CXX_LDS
+    return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(qg_smem4) + a);
+#else
     float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a + smem_base()));
     return v;
+#endif
+}
+
+// ---------------------------------------------------------------------------
+// mbarriers and bulk (TMA engine) copies.  Every wait is bounded in time: a
+// wait that has not completed after kWaitNs returns false and the caller
+// records QSTATUS_DEVICE_TIMEOUT and leaves.
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase of the given parity to complete; false after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory; completion is counted on
+// mbarrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
 // Bytes of one ring slot: NR chunk rows x 32 lanes (16 B of codes, int3 also
@@ -466,7 +575,9 @@ __host__ __device__ constexpr int ring_slot_bytes()
 // ---------------------------------------------------------------------------
 // Row streaming.  A warp processes row tiles of R rows (of NM matrices sharing
 // the same row index: NM = 2 for gate and up): tiles tile_first,
-// tile_first + tile_step, ... below ntiles, rows row0 + tile * R + r < row_end.
+// tile_first + tile_step, ... below ntiles, rows row0 + tile * R + r < row_end;
+// rows of the last tile past row_end are not copied (their arithmetic runs on
+// stale ring data and the sink drops it, which keeps the rows interleaved).
 // Work is the flattened sequence (tile, step); step c covers chunk c*32 + lane
 // of each row.  Copies run P steps ahead of use through a ring of P slots in
 // this warp's part of shared memory.  Each row's chunk and scale addresses are
@@ -474,7 +585,7 @@ __host__ __device__ constexpr int ring_slot_bytes()
 // once per finished tile from every lane: sink(value, index, lane_holds_it,
 // first row of the tile, row_end) with index v = (s * R + r) * NM + m.
 // ---------------------------------------------------------------------------
-template <int FMT, int S, int R, int P, int NM>
+template <int FMT, int S, int R, int P, int NM, bool LOOP_S = false>
 struct RowStreamer {
     static constexpr int EPL = Traits<FMT>::EPL;
     static constexpr int NR = NM * R;
@@ -487,19 +598,29 @@ struct RowStreamer {
     const uint8_t* bp[NR];    // int3 plane B
     const float* sp[NR];      // this lane's next scale of each row
     int sstep;                // scale advance per step
-    uint32_t ring;            // this lane's byte position in slot 0 of the warp's ring
+    uint32_t ring;            // this lane's byte offset in slot 0 of the warp's ring
+    uint32_t sbase;           // shared-window address of the dynamic shared memory
 
     Mat mats[NM];
     long long row0, row_end;
     int it_tile, it_c, ct_tile, ct_c;
+    int it_valid;             // rows of the issuing tile below row_end
     int total, issued, nchunks, nsteps, ntiles, tile_step, lane;
+
+    __device__ __forceinline__ int tile_rows(int tile) const
+    {
+        const long long first = row0 + (long long)tile * R;
+        return (int)(row_end - first < R ? row_end - first : R);
+    }
 
     __device__ __forceinline__ void set_tile(int tile)
     {
+        const long long first = row0 + (long long)tile * R;
+        it_valid = tile_rows(tile);
 #pragma unroll
         for (int r = 0; r < R; r++) {
-            long long o = row0 + (long long)tile * R + r;
-            o = o < row_end ? o : row_end - 1;       // tail rows: load a valid row, drop the result
+            long long o = first + r;
+            o = o < row_end ? o : row_end - 1;       // rows past the end are never loaded
 #pragma unroll
             for (int m = 0; m < NM; m++) {
                 const Mat& M = mats[m];
@@ -525,10 +646,10 @@ struct RowStreamer {
     {
         if (issued < total) {
             const bool ok = it_c * 32 + lane < nchunks;
-            const uint32_t slot = ring + (uint32_t)(p * SLOT);
+            const uint32_t slot = sbase + ring + (uint32_t)(p * SLOT);
 #pragma unroll
             for (int rr = 0; rr < NR; rr++) {
-                if (ok) {
+                if (ok && (rr % R) < it_valid) {
                     cp_async16(slot + rr * 512, wp[rr]);
                     if constexpr (FMT == FMT_INT3_G64) cp_async8(slot + B_OFF + rr * 256 - lane * 8, bp[rr]);
                     cp_async4(slot + S_OFF + rr * 128 - lane * 12, sp[rr]);
@@ -547,7 +668,7 @@ struct RowStreamer {
         cp_async_commit();
     }
 
-    // ring_warp: shared address of this warp's ring (P slots of SLOT bytes).
+    // ring_warp: byte offset of this warp's ring (P slots of SLOT bytes).
     __device__ __forceinline__ void begin(const Mat* m, long long row0_, long long row_end_, int tile_first,
                                           int ntiles_, int tile_step_, int lane_, uint32_t ring_warp)
     {
@@ -559,6 +680,7 @@ struct RowStreamer {
         tile_step = tile_step_;
         ntiles = ntiles_;
         ring = ring_warp + (uint32_t)lane * 16;
+        sbase = smem_base();
         nchunks = m[0].I / EPL;
         nsteps = (nchunks + 31) / 32;
         // int8: one scale per row; int4: 32 chunks span 32 >> gsh groups
@@ -573,9 +695,10 @@ struct RowStreamer {
         for (int p = 0; p < P; p++) issue(p);
     }
 
-    // xs[s]: shared-memory addresses of the swizzled activation rows.
+    // xs[s]: shared-memory byte offsets of the swizzled activation rows; only
+    // the first s_act (<= S) are in use.
     template <class Sink>
-    __device__ __forceinline__ void run(const uint32_t (&xs)[S], Sink& sink)
+    __device__ __forceinline__ void run(const uint32_t (&xs)[S], int s_act, Sink& sink)
     {
         const uint32_t swz = (uint32_t)x_swz(EPL, lane);
         uint32_t xo[8];
@@ -585,11 +708,11 @@ struct RowStreamer {
 #pragma unroll
         for (int s = 0; s < S; s++) xl[s] = xs[s] + (uint32_t)lane * (EPL * 4);
 
-        float acc[NR][S];
+        float acc[S][NR];
 #pragma unroll
-        for (int rr = 0; rr < NR; rr++)
+        for (int s = 0; s < S; s++)
 #pragma unroll
-            for (int s = 0; s < S; s++) acc[rr][s] = 0.f;
+            for (int rr = 0; rr < NR; rr++) acc[s][rr] = 0.f;
 
         for (int j0 = 0; j0 < total; j0 += P) {
 #pragma unroll
@@ -613,26 +736,54 @@ struct RowStreamer {
                         uint32_t xq[S];
 #pragma unroll
                         for (int s = 0; s < S; s++) xq[s] = xl[s] + (uint32_t)ct_c * (32 * EPL * 4);
-                        consume<FMT, S, NR>(c, sc, xq, xo, acc);
+                        if constexpr (LOOP_S) {
+                            // one-row arithmetic per activation row in use, on the same ring data
+#pragma unroll
+                            for (int s = 0; s < S; s++) {
+                                if (s < s_act) {
+                                    const uint32_t x1[1] = {xq[s]};
+                                    consume<FMT, 1, NR>(c, sc, x1, xo,
+                                                        reinterpret_cast<float(&)[1][NR]>(acc[s]), 1);
+                                }
+                            }
+                        } else {
+                            consume<FMT, S, NR>(c, sc, xq, xo, acc, s_act);
+                        }
                     }
                     issue(p);
                     if (++ct_c == nsteps) {
                         // finished tile ct_tile: reduce and hand to the sink
-                        float v[V];
+                        if (LOOP_S && s_act == 1) {
+                            // one activation row in use: reduce only its NR values
+                            constexpr int V1 = pow2_ceil(R * NM);
+                            float v[V1];
 #pragma unroll
-                        for (int i = 0; i < V; i++) v[i] = 0.f;
-#pragma unroll
-                        for (int s = 0; s < S; s++)
+                            for (int i = 0; i < V1; i++) v[i] = 0.f;
 #pragma unroll
                             for (int r = 0; r < R; r++)
 #pragma unroll
-                                for (int m = 0; m < NM; m++) {
-                                    v[(s * R + r) * NM + m] = acc[m * R + r][s];
-                                    acc[m * R + r][s] = 0.f;
-                                }
-                        const float red = warp_reduce_scatter<V>(v, lane);
-                        const int idx = reduce_scatter_index<V>(lane);
-                        sink(red, idx, lane < V, row0 + (long long)ct_tile * R, row_end);
+                                for (int m = 0; m < NM; m++) v[r * NM + m] = acc[0][m * R + r];
+                            const float red = warp_reduce_scatter<V1>(v, lane);
+                            const int idx = reduce_scatter_index<V1>(lane);
+                            sink.template put<V1>(red, idx, lane < V1, row0 + (long long)ct_tile * R, row_end);
+                        } else {
+                            float v[V];
+#pragma unroll
+                            for (int i = 0; i < V; i++) v[i] = 0.f;
+#pragma unroll
+                            for (int s = 0; s < S; s++)
+#pragma unroll
+                                for (int r = 0; r < R; r++)
+#pragma unroll
+                                    for (int m = 0; m < NM; m++) v[(s * R + r) * NM + m] = acc[s][m * R + r];
+                            const float red = warp_reduce_scatter<V>(v, lane);
+                            const int idx = reduce_scatter_index<V>(lane);
+                            sink.template put<V>(red, idx, lane < V, row0 + (long long)ct_tile * R, row_end);
+                        }
+#pragma unroll
+                        for (int s = 0; s < S; s++)
+#pragma unroll
+                            for (int rr = 0; rr < NR; rr++) acc[s][rr] = 0.f;
                         ct_c = 0;
                         ct_tile += tile_step;
                     }

@@ -70,16 +70,17 @@ struct RingLayout {
     int ring_stride;
 };
 
-// Ring bytes per warp: kRing slots sized for the largest tile of the family
-// (one activation row).
-template <int NM>
+// Ring bytes per warp: kRing slots sized for the tiles of S activation rows.
+template <int NM, int S = 1>
 __host__ __device__ constexpr int ring_stride_bytes()
 {
-    return kRing * ring_slot_bytes<FMT, NM * rows_per_tile<1, NM>()>();
+    return kRing * ring_slot_bytes<FMT, NM * rows_per_tile<S, NM>()>();
 }
 
 template <int NM>
 struct DenseJob : RingLayout {
+    static constexpr bool kLoopS = false;     // activation rows share each decoded word
+    BulkLayout bulk;
     Mat m[NM];
     const float* x;      // [S][I]
     float* y;            // y[s * ldy + row]
@@ -97,11 +98,16 @@ struct DenseJob : RingLayout {
     }
     __device__ const float* xrow(int, int s) const { return x + (long long)s * m[0].I; }
     __device__ void store(int, int s, long long row, float v) const { y[(long long)s * ldy + row] = v; }
+    __device__ int width() const { return m[0].I; }
+    __device__ int* status_word() const { return nullptr; }
 };
 
 // Expert phase A: the gate and up rows of every used expert, against the
 // tokens routed to it; stores h = silu(g) * u per sorted pair.
 struct ExpertUpJob : RingLayout {
+    static constexpr bool kLoopS = true;      // one-pair tiles, one pass of arithmetic per pair
+    BulkLayout bulk;
+    int* status;
     Mat gate0, up0;                 // expert 0's matrices (w, sc advanced per expert)
     long long mat_bytes, mat_scales;
     const float* x;
@@ -130,11 +136,16 @@ struct ExpertUpJob : RingLayout {
     {
         h[(long long)(batches[b].y + s) * F + row] = v;
     }
+    __device__ int width() const { return D; }
+    __device__ int* status_word() const { return status; }
 };
 
 // Expert phase B: the down rows of every used expert against the h vectors of
 // its pairs; stores z = down h per sorted pair.
 struct ExpertDownJob : RingLayout {
+    static constexpr bool kLoopS = true;
+    BulkLayout bulk;
+    int* status;
     Mat down0;
     long long mat_bytes, mat_scales;
     const int32_t* hdr;
@@ -159,83 +170,77 @@ struct ExpertDownJob : RingLayout {
     {
         z[(long long)(batches[b].y + s) * D + row] = v;
     }
+    __device__ int width() const { return F; }
+    __device__ int* status_word() const { return status; }
 };
 
-// Hands finished tiles to the job (NM = 2: h = silu(gate) * up).
+// Hands finished tiles to the job (NM = 2: h = silu(gate) * up).  A reduced
+// value with index v = (s * R + r) * NM + m belongs to activation row s, tile
+// row r, matrix m; V is the (power-of-two) count that was reduced.
 template <class Job, int S, int R, int NM>
 struct Sink {
     const Job& job;
     int b;
-    __device__ __forceinline__ void operator()(float v, int idx, bool lane_ok, long long tile_row0,
-                                               long long row_end) const
+    int s_act;
+    template <int V>
+    __device__ __forceinline__ void put(float v, int idx, bool lane_ok, long long tile_row0, long long row_end) const
     {
-        constexpr int V = pow2_ceil(S * R * NM);
         if constexpr (NM == 2) {
             const float u = __shfl_xor_sync(0xffffffffu, v, V / 2);
             if (lane_ok && !(idx & 1) && idx < S * R * 2) {
                 const int sr = idx >> 1, s = sr / R, r = sr - (sr / R) * R;
                 const long long row = tile_row0 + r;
-                if (row < row_end) job.store(b, s, row, v / (1.0f + expf(-v)) * u);
+                if (row < row_end && s < s_act) job.store(b, s, row, v / (1.0f + expf(-v)) * u);
             }
         } else {
             if (lane_ok && idx < S * R) {
                 const int s = idx / R, r = idx - (idx / R) * R;
                 const long long row = tile_row0 + r;
-                if (row < row_end) job.store(b, s, row, v);
+                if (row < row_end && s < s_act) job.store(b, s, row, v);
             }
         }
     }
 };
 
-// One segment: rows [l0, l1) of batch b, all warps of the CTA.  Not inlined,
-// so a kernel that dispatches over several S gets a register allocation per S.
+// One segment: rows [l0, l1) of batch b, all warps of the CTA, with the
+// batch's s_act <= S activation rows; warp w takes the row tiles w, w + W, ...
 template <int NM, int S, class Job>
-__device__ __noinline__ void segment(const Job job, int b, long long l0, long long l1, float* xs, int& staged)
+__device__ __forceinline__ void segment(const Job& job, int b, long long l0, long long l1, int s_act, float* xs,
+                                        int& staged)
 {
-    constexpr int R = rows_per_tile<S, NM>();
+    constexpr int R = rows_per_tile<Job::kLoopS ? 1 : S, NM>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Mat m[NM];
     job.mats(b, m);
+    RowStreamer<FMT, S, R, kRing, NM, Job::kLoopS> st;
     const int ntiles = (int)((l1 - l0 + R - 1) / R);
-    RowStreamer<FMT, S, R, kRing, NM> st;
-    const uint32_t base = (uint32_t)__cvta_generic_to_shared(xs);
-    st.begin(m, l0, l1, warp, ntiles, kWarps, lane,
-             base + (uint32_t)(job.ring_off + warp * job.ring_stride));   // copies in flight during staging
+    st.begin(m, l0, l1, warp, ntiles, (int)(blockDim.x >> 5), lane,
+             (uint32_t)(job.ring_off + warp * job.ring_stride));   // copies in flight during staging
     const int I = m[0].I;
     if (b != staged) {
         __syncthreads();
         const float* src[S];
 #pragma unroll
-        for (int s = 0; s < S; s++) src[s] = job.xrow(b, s);
-        stage_rows<EPL>(xs, I, src, S, I);
+        for (int s = 0; s < S; s++) src[s] = job.xrow(b, s < s_act ? s : 0);
+        stage_rows<EPL>(xs, I, src, s_act, I);
         __syncthreads();
         staged = b;
     }
     uint32_t xsh[S];
 #pragma unroll
-    for (int s = 0; s < S; s++) xsh[s] = base + (uint32_t)(s * I) * 4u;
-    Sink<Job, S, R, NM> sink{job, b};
-    st.run(xsh, sink);
-}
-
-template <int NM, int S, int SMAX, class Job>
-__device__ __forceinline__ void segment_dispatch(int Sr, const Job& job, int b, long long l0, long long l1,
-                                                 float* xs, int& staged)
-{
-    if constexpr (S <= SMAX) {
-        if (Sr == S) segment<NM, S>(job, b, l0, l1, xs, staged);
-        else segment_dispatch<NM, S + 1, SMAX>(Sr, job, b, l0, l1, xs, staged);
-    }
+    for (int s = 0; s < S; s++) xsh[s] = (uint32_t)(s * I) * 4u;   // byte offsets: x rows start at 0
+    Sink<Job, S, R, NM> sink{job, b, s_act};
+    st.run(xsh, s_act, sink);
 }
 
 // The streaming kernel: CTA c takes the rows [N c / G, N (c+1) / G) of the
 // job's batches laid end to end (N = batches * rows per batch), so every SM
 // gets the same number of weight rows; the range splits into segments where
-// the batch (and so the staged activation set) changes.
-template <int NM, int SMIN, int SMAX, class Job>
-__global__ void __launch_bounds__(kThreads, 1) k_stream(const Job job)
+// the batch (and so the staged activation set) changes.  S is the number of
+// activation rows the code is built for; a batch may use fewer.
+template <int NM, int S, class Job>
+__global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ Job job)
 {
-    extern __shared__ float4 qg_smem4[];
     float* xs = reinterpret_cast<float*>(qg_smem4);
     if (job.bad()) return;
     const long long rows_per = job.rows_per();
@@ -249,11 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const Job job)
         const long long base = (long long)b * rows_per;
         const long long l0 = r - base;
         const long long l1 = (r_end - base) < rows_per ? (r_end - base) : rows_per;
-        const int S = job.batch_S(b);
-        segment_dispatch<NM, SMIN, SMAX>(S, job, b, l0, l1, xs, staged);
+        segment<NM, S>(job, b, l0, l1, job.batch_S(b), xs, staged);
         r = base + l1;
     }
 }
+
+#include "qg_bulk.cuh"
 
 // ---------------------------------------------------------------------------
 // Dequantization: one thread per chunk, the same decoding arithmetic as the
@@ -342,29 +348,108 @@ static cudaError_t set_smem(K kernel, size_t bytes, int (&granted)[64])
     return e;
 }
 
-template <int NM, int S>
-static cudaError_t launch_dense(const DenseJob<NM>& job, int grid, size_t smem, cudaStream_t st)
+#ifndef QG_BULK
+#define QG_BULK 0
+#endif
+
+static int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Plans the bulk-copy kernel for rows of I inputs, NM matrices per tile, R
+// rows per tile and x_bytes of activation rows.  False when the shapes do not
+// allow it (scale rows or int3 plane-B rows not a multiple of 16 bytes) or
+// fewer than two stages fit; the per-lane copy kernel then runs instead.
+#ifndef QG_BULK_STAGE
+#define QG_BULK_STAGE 65536
+#endif
+#ifndef QG_BULK_NSTAGE
+#define QG_BULK_NSTAGE 4
+#endif
+static bool plan_bulk(int NM, int R, int I, int gs, size_t x_bytes, BulkLayout& L)
 {
-    auto kern = k_stream<NM, S, S, DenseJob<NM>>;
+    if (!QG_BULK) return false;
+    L.rb = FMT == FMT_INT8_ROW ? I : (FMT == FMT_INT3_G64 ? I / 4 : I / 2);
+    L.rbB = FMT == FMT_INT3_G64 ? I / 8 : 0;
+    L.sb = FMT == FMT_INT8_ROW ? 0 : (I / gs) * 4;
+    if (L.rb % 16 || L.rbB % 16 || L.sb % 16) return false;
+    const int nchunks = I / EPL;
+    const int nsteps = (nchunks + 31) / 32;
+    L.kp = (nsteps + 3) / 4;
+    L.kpw = (nsteps + L.kp - 1) / L.kp;
+    L.kp = (nsteps + L.kpw - 1) / L.kpw;
+    const int row_bytes = NM * (L.rb + L.rbB + L.sb);
+    const int tile_bytes = R * row_bytes;
+    const int x_end = align_up((int)x_bytes, 128);
+    // Largest stage (up to QG_BULK_STAGE bytes) that leaves room for at
+    // least three stages, else two.
+    for (int min_ns = 3; min_ns >= 2; min_ns--) {
+        for (int tps = QG_BULK_STAGE / tile_bytes > 0 ? QG_BULK_STAGE / tile_bytes : 1; tps >= 1; tps--) {
+            L.rs = tps * R;
+            L.stage_bytes = align_up(L.rs * row_bytes, 128);
+            L.stage_off = x_end;
+            for (int ns = QG_BULK_NSTAGE; ns >= min_ns; ns--) {
+                L.nstage = ns;
+                L.part_off = L.stage_off + ns * L.stage_bytes;
+                L.cnt_off = L.part_off + ns * tps * L.kp * 32 * 4;
+                L.bar_off = align_up(L.cnt_off + ns * tps * 4, 8);
+                L.total = L.bar_off + (2 * ns + 1) * 8;
+                if (L.total <= kSmemMax) {
+                    int off = 0;
+                    for (int m = 0; m < NM; m++) { L.w_off[m] = off; off += L.rs * L.rb; }
+                    for (int m = 0; m < NM; m++) { L.b_off[m] = off; off += L.rs * L.rbB; }
+                    for (int m = 0; m < NM; m++) { L.s_off[m] = off; off += L.rs * L.sb; }
+                    for (int m = NM; m < 2; m++) L.w_off[m] = L.b_off[m] = L.s_off[m] = 0;
+                    return true;
+                }
+            }
+        }
+    }
+    return false;
+}
+
+template <class K>
+static cudaError_t set_smem_max(K kernel, int (&granted)[64])
+{
+    return set_smem(kernel, (size_t)kSmemMax, granted);
+}
+
+template <int NM, int S>
+static cudaError_t launch_dense(const DenseJob<NM>& job_in, int grid, size_t x_bytes, cudaStream_t st)
+{
+    DenseJob<NM> job = job_in;
+    constexpr int R = rows_per_tile<S, NM>();
+    const int gs = FMT == FMT_INT8_ROW ? job.m[0].I : job.m[0].I / job.m[0].ngrp;
+    bool scales16 = true;
+    for (int k = 0; k < NM; k++) scales16 = scales16 && (reinterpret_cast<uintptr_t>(job.m[k].sc) & 15) == 0;
+    if (scales16 && plan_bulk(NM, R, job.m[0].I, gs, (size_t)S * job.m[0].I * sizeof(float), job.bulk)) {
+        auto kb = k_bulk<NM, S, DenseJob<NM>>;
+        static int granted_b[64];
+        cudaError_t e = set_smem_max(kb, granted_b);
+        if (e != cudaSuccess) return e;
+        kb<<<grid, (kBulkConsumers + 1) * 32, job.bulk.total, st>>>(job);
+        return cudaGetLastError();
+    }
+    auto kern = k_stream<NM, S, DenseJob<NM>>;
+    const int warps = kWarps;
+    const size_t smem = x_bytes + (size_t)warps * job.ring_stride;
     static int granted[64];
-    cudaError_t e = set_smem(kern, smem, granted);
+    cudaError_t e = set_smem(kern, (size_t)x_bytes + (size_t)kWarps * job.ring_stride, granted);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(job);
+    kern<<<grid, warps * 32, smem, st>>>(job);
     return cudaGetLastError();
 }
 
 template <int NM>
-static cudaError_t launch_dense_s(const DenseJob<NM>& job, int s, int grid, size_t smem, cudaStream_t st)
+static cudaError_t launch_dense_s(const DenseJob<NM>& job, int s, int grid, size_t x_bytes, cudaStream_t st)
 {
     switch (s) {
-    case 1: return launch_dense<NM, 1>(job, grid, smem, st);
-    case 2: return launch_dense<NM, 2>(job, grid, smem, st);
-    case 3: return launch_dense<NM, 3>(job, grid, smem, st);
-    case 4: return launch_dense<NM, 4>(job, grid, smem, st);
-    case 5: return launch_dense<NM, 5>(job, grid, smem, st);
-    case 6: return launch_dense<NM, 6>(job, grid, smem, st);
-    case 7: return launch_dense<NM, 7>(job, grid, smem, st);
-    case 8: return launch_dense<NM, 8>(job, grid, smem, st);
+    case 1: return launch_dense<NM, 1>(job, grid, x_bytes, st);
+    case 2: return launch_dense<NM, 2>(job, grid, x_bytes, st);
+    case 3: return launch_dense<NM, 3>(job, grid, x_bytes, st);
+    case 4: return launch_dense<NM, 4>(job, grid, x_bytes, st);
+    case 5: return launch_dense<NM, 5>(job, grid, x_bytes, st);
+    case 6: return launch_dense<NM, 6>(job, grid, x_bytes, st);
+    case 7: return launch_dense<NM, 7>(job, grid, x_bytes, st);
+    case 8: return launch_dense<NM, 8>(job, grid, x_bytes, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -384,7 +469,7 @@ cudaError_t QG_CAT(gemv_, QG_NAME)(const HostMat& hm, const float* x, int s, flo
     job.S = s;
     job.ring_off = (int)align16((size_t)s * hm.I * sizeof(float));
     job.ring_stride = ring_stride_bytes<1>();
-    return launch_dense_s<1>(job, s, grid, job.ring_off + (size_t)kWarps * job.ring_stride, st);
+    return launch_dense_s<1>(job, s, grid, job.ring_off, st);
 }
 
 cudaError_t QG_CAT(gate_up_, QG_NAME)(const HostMat& g, const HostMat& u, const float* x, int s, float* h,
@@ -399,7 +484,7 @@ cudaError_t QG_CAT(gate_up_, QG_NAME)(const HostMat& g, const HostMat& u, const 
     job.S = s;
     job.ring_off = (int)align16((size_t)s * g.I * sizeof(float));
     job.ring_stride = ring_stride_bytes<2>();
-    return launch_dense_s<2>(job, s, grid, job.ring_off + (size_t)kWarps * job.ring_stride, st);
+    return launch_dense_s<2>(job, s, grid, job.ring_off, st);
 }
 
 cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st)
@@ -421,8 +506,19 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
     job.D = a.D;
     job.F = a.F;
     job.ring_off = (int)align16((size_t)a.smax * a.D * sizeof(float));
-    job.ring_stride = ring_stride_bytes<2>();
-    auto kern = k_stream<2, 1, kSmax, ExpertUpJob>;
+    job.ring_stride = ring_stride_bytes<2, 1>();
+    job.status = a.status_dev;
+    const bool scales16 = ((reinterpret_cast<uintptr_t>(a.gate_s) | reinterpret_cast<uintptr_t>(a.up_s)) & 15) == 0;
+    if (scales16 &&
+        plan_bulk(2, rows_per_tile<1, 2>(), a.D, gs, (size_t)a.smax * a.D * sizeof(float), job.bulk)) {
+        auto kb = k_bulk<2, kExpertSmax, ExpertUpJob>;
+        static int granted_b[64];
+        cudaError_t e = set_smem_max(kb, granted_b);
+        if (e != cudaSuccess) return e;
+        kb<<<grid, (kBulkConsumers + 1) * 32, job.bulk.total, st>>>(job);
+        return cudaGetLastError();
+    }
+    auto kern = k_stream<2, kExpertSmax, ExpertUpJob>;
     const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
     static int granted[64];
     cudaError_t e = set_smem(kern, smem, granted);
@@ -448,14 +544,36 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
     job.D = a.D;
     job.F = a.F;
     job.ring_off = (int)align16((size_t)a.smax * a.F * sizeof(float));
-    job.ring_stride = ring_stride_bytes<1>();
-    auto kern = k_stream<1, 1, kSmax, ExpertDownJob>;
+    job.ring_stride = ring_stride_bytes<1, 1>();
+    job.status = a.status_dev;
+    const bool scales16 = (reinterpret_cast<uintptr_t>(a.down_s) & 15) == 0;
+    if (scales16 &&
+        plan_bulk(1, rows_per_tile<1, 1>(), a.F, gs, (size_t)a.smax * a.F * sizeof(float), job.bulk)) {
+        auto kb = k_bulk<1, kExpertSmax, ExpertDownJob>;
+        static int granted_b[64];
+        cudaError_t e = set_smem_max(kb, granted_b);
+        if (e != cudaSuccess) return e;
+        kb<<<grid, (kBulkConsumers + 1) * 32, job.bulk.total, st>>>(job);
+        return cudaGetLastError();
+    }
+    auto kern = k_stream<1, kExpertSmax, ExpertDownJob>;
     const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
     static int granted[64];
     cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(job);
     return cudaGetLastError();
+}
+
+int QG_CAT(device_error_, QG_NAME)(int clear)
+{
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bulk_error, sizeof(int)) != cudaSuccess) return QSTATUS_LAUNCH;
+    if (clear && v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_bulk_error, &zero, sizeof(int));
+    }
+    return v;
 }
 
 size_t QG_CAT(ring_bytes_, QG_NAME)(int nm)

@@ -15,7 +15,12 @@ namespace qg {
 #endif
 constexpr int kWarps = QG_WARPS;            // warps per CTA of the streaming kernels
 constexpr int kThreads = kWarps * 32;
-constexpr int kSmax = 8;                    // activation rows per launch / per expert batch
+#ifndef QG_BULK_CONSUMERS
+#define QG_BULK_CONSUMERS 16
+#endif
+constexpr int kBulkConsumers = QG_BULK_CONSUMERS;   // consumer warps of the bulk-copy kernels
+constexpr int kSmax = 8;                    // activation rows per dense launch
+constexpr int kExpertSmax = 4;              // (token, rank) pairs per expert batch
 constexpr int kSmemMax = 227 * 1024;        // dynamic shared memory per CTA (sm_103a)
 constexpr int kMaxPairs = 4096;             // s * k limit of qexpert_group
 
@@ -71,6 +76,18 @@ struct ExpertArgs {
     int smax;          // pairs per batch
 };
 
+// Shared-memory plan of a bulk-copy launch (byte offsets from the start of
+// dynamic shared memory; the activation rows sit at offset 0).
+struct BulkLayout {
+    int rs;            // rows per stage
+    int nstage;        // stages in the ring
+    int kp;            // work units per row tile (K parts)
+    int kpw;           // warp steps per work unit
+    int stage_off, stage_bytes, part_off, cnt_off, bar_off, total;
+    int w_off[2], b_off[2], s_off[2];   // per matrix, inside a stage
+    int rb, rbB, sb;   // bytes per row: codes (int3: plane A), int3 plane B, scales (0: read from global)
+};
+
 // Per-format launchers (defined in qg_fmt_<format>.cu).  Each returns a
 // cudaError_t of the launch.
 #define QG_DECLARE_FMT(name)                                                                            \
@@ -81,7 +98,8 @@ struct ExpertArgs {
     cudaError_t expert_up_##name(const ExpertArgs& a, int grid, cudaStream_t st);                       \
     cudaError_t expert_down_##name(const ExpertArgs& a, int grid, cudaStream_t st);                     \
     cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);                         \
-    size_t ring_bytes_##name(int nm);
+    size_t ring_bytes_##name(int nm);                                                                 \
+    int device_error_##name(int clear);
 
 QG_DECLARE_FMT(int8)
 QG_DECLARE_FMT(int4)
