@@ -185,6 +185,20 @@ const char* qlast_cuda_error(void);
  */
 int qdevice_error(int clear);
 
+/*
+ * Kernel choice for the streaming launches of this process (a tuning and
+ * testing knob; the surveyed pages have no counterpart).  QKERNEL_AUTO picks
+ * per shape; QKERNEL_RING forces the per-lane copy kernel; QKERNEL_TILE the
+ * tensor-copy tile kernel wherever its plan fits (else the ring kernel).  Both
+ * kernels give the same bits.  Returns the previous policy, or
+ * QSTATUS_BAD_FMT for an unknown one (the policy is then unchanged).  Not
+ * synchronized with launches in flight on other threads.
+ */
+#define QKERNEL_AUTO 0
+#define QKERNEL_RING 1
+#define QKERNEL_TILE 2
+int qkernel_policy(int policy);
+
 #ifdef __cplusplus
 }
 #endif

@@ -99,3 +99,14 @@ def test_expert_group_checks(L):
     bad[10] = 2050                                     # F not a multiple of the group
     assert L.qexpert_group(*bad) == -2
     assert _lib.qexpert_group_workspace(0, 6144, 2048, 8, 8) >= 0
+
+
+def test_kernel_policy_round_trip(L):
+    """The kernel-choice knob is host state only: set, read back, reject unknown values."""
+    prev = _lib.qkernel_policy(_lib.QKERNEL_TILE)
+    try:
+        assert _lib.qkernel_policy(_lib.QKERNEL_RING) == _lib.QKERNEL_TILE
+        assert L.qkernel_policy(7) == -1            # QSTATUS_BAD_FMT, policy unchanged
+        assert _lib.qkernel_policy(_lib.QKERNEL_AUTO) == _lib.QKERNEL_RING
+    finally:
+        _lib.qkernel_policy(prev)

@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.qlast_cuda_error.restype = ctypes.c_char_p
         L.qdevice_error.argtypes = [I]
         L.qdevice_error.restype = I
+        L.qkernel_policy.argtypes = [I]
+        L.qkernel_policy.restype = I
         _lib = L
     return _lib
 
@@ -99,6 +101,17 @@ def _check(status: int):
 
 def qstatus_string(status: int) -> str:
     return lib().qstatus_string(status).decode()
+
+
+QKERNEL_AUTO, QKERNEL_RING, QKERNEL_TILE = 0, 1, 2
+
+
+def qkernel_policy(policy: int) -> int:
+    """Sets the process's kernel choice (QKERNEL_*); returns the previous one."""
+    prev = lib().qkernel_policy(int(policy))
+    if prev < 0:
+        raise QStatusError(prev, qstatus_string(prev))
+    return prev
 
 
 def qdevice_error(clear: bool = False) -> int:

@@ -1,6 +1,7 @@
 // qg_abi.cu -- the C entry points: argument checks, launch set-up, and the
 // format-independent kernels of the routed-expert group (grouping the
 // (token, rank) pairs by expert, and the rank-order weighted sum).
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda_runtime.h>
@@ -10,6 +11,9 @@
 namespace qg {
 
 static thread_local const char* g_last_cuda_error = "no error";
+
+static std::atomic<int> g_kernel_policy{QKERNEL_AUTO};
+int kernel_policy() { return g_kernel_policy.load(std::memory_order_relaxed); }
 
 static int launch_status(cudaError_t e)
 {
@@ -186,6 +190,43 @@ cudaError_t expert_combine(const ExpertArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against
+// the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn()
+{
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long long row_bytes, int box_bytes,
+                     int box_rows, bool f32)
+{
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || rows <= 0 || row_bytes <= 0 || row_bytes % 16 || box_bytes % 16 || box_bytes > 1024 ||
+        box_rows < 1 || box_rows > 256 || !aligned(base, 16))
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 4), (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace qg
 
 using namespace qg;
@@ -210,6 +251,12 @@ const char* qstatus_string(int status)
 }
 
 const char* qlast_cuda_error(void) { return g_last_cuda_error; }
+
+int qkernel_policy(int policy)
+{
+    if (policy != QKERNEL_AUTO && policy != QKERNEL_RING && policy != QKERNEL_TILE) return QSTATUS_BAD_FMT;
+    return g_kernel_policy.exchange(policy);
+}
 
 int qdevice_error(int clear)
 {

@@ -277,7 +277,19 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int j)
 // of a word shared by all NR rows; with several, a word is decoded once for
 // all of them.
 // ---------------------------------------------------------------------------
-template <int FMT, int S, int NR>
+// Shared-memory address of quad qd (0 .. EPL/4 - 1) of a lane's x segment.
+// Swizzled layout: the segment is contiguous from xq, quads placed by xo.
+// Lane-interleaved layout (PERM): quad qd of the 32 lanes of a warp step are
+// 32 consecutive float4, so xq is the lane's quad 0 and quad qd sits 512 bytes
+// per quad further.
+template <bool PERM>
+__device__ __forceinline__ uint32_t x_quad(uint32_t xq, const uint32_t (&xo)[8], int qd)
+{
+    if constexpr (PERM) return xq + 512u * (uint32_t)qd;
+    else return xq + ((uint32_t)(qd >> 3) << 7) + xo[qd & 7];
+}
+
+template <int FMT, int S, int NR, bool PERM = false>
 __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (&sc)[NR],
                                         const uint32_t (&xq)[S], const uint32_t (&xo)[8], float (&acc)[S][NR],
                                         int s_act)
@@ -295,8 +307,8 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             if constexpr (S == 1) {
-                const float4 xa = lds4s(xq[0] + xo[2 * j]);
-                const float4 xc = lds4s(xq[0] + xo[2 * j + 1]);
+                const float4 xa = lds4s(x_quad<PERM>(xq[0], xo, 2 * j));
+                const float4 xc = lds4s(x_quad<PERM>(xq[0], xo, 2 * j + 1));
 #pragma unroll
                 for (int rr = 0; rr < NR; rr++) {
                     float2 d[4];
@@ -317,8 +329,8 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
 #pragma unroll
                 for (int s = 0; s < S; s++) {
                     if (s >= s_act) break;                       // warp-uniform: activation rows in use
-                    const float4 xa = lds4s(xq[s] + xo[2 * j]);
-                    const float4 xc = lds4s(xq[s] + xo[2 * j + 1]);
+                    const float4 xa = lds4s(x_quad<PERM>(xq[s], xo, 2 * j));
+                    const float4 xc = lds4s(x_quad<PERM>(xq[s], xo, 2 * j + 1));
 #pragma unroll
                     for (int rr = 0; rr < NR; rr++) {
                             part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
@@ -340,7 +352,7 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
 #pragma unroll
             for (int s = 0; s < S; s++) {
                 if (s >= s_act) break;
-                const float4 xa = lds4s(xq[s] + xo[j]);
+                const float4 xa = lds4s(x_quad<PERM>(xq[s], xo, j));
 #pragma unroll
                 for (int rr = 0; rr < NR; rr++) {
                     part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
@@ -368,7 +380,7 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
 #pragma unroll
                 for (int s = 0; s < S; s++) {
                     if (s >= s_act) break;
-                    const float4 xv = lds4s(xq[s] + (qd >= 8 ? 128u : 0u) + xo[qd & 7]);
+                    const float4 xv = lds4s(x_quad<PERM>(xq[s], xo, qd));
 #pragma unroll
                     for (int rr = 0; rr < NR; rr++) {
                             part[rr][s] = ffma2(d[rr][0], make_float2(xv.x, xv.y), part[rr][s]);
@@ -400,21 +412,28 @@ __device__ __forceinline__ void stage_rows(float* xs, int xstride, const float* 
     }
 }
 
-__host__ __device__ constexpr int ilog2(int v) { int l = 0; while ((1 << l) < v) l++; return l; }
-
-// The same staging done by threads [0, nthreads) only (t = this thread).
+// The same rows in the lane-interleaved layout, rows of xstride floats (a
+// multiple of 32 * EPL) zero beyond I: element i of chunk q = i / EPL (lane
+// l = q % 32 of warp step k = q / 32), quad j of the chunk, goes to float4
+// (k * EPL / 4 + j) * 32 + l.  Threads t of [0, nthreads) take part.
 template <int EPL>
-__device__ __forceinline__ void stage_rows_part(float* xs, int xstride, const float* const* src, int nrows, int I,
+__device__ __forceinline__ void stage_rows_perm(float* xs, int xstride, const float* const* src, int nrows, int I,
                                                 int t, int nthreads)
 {
-    const int nq = I / 4;
+    constexpr int QPC = EPL / 4;              // quads per chunk
+    const int nq = xstride / 4, iq = I / 4;
     for (int idx = t; idx < nrows * nq; idx += nthreads) {
         const int s = idx / nq;
         const int qd = idx - s * nq;
-        const float4 v = *reinterpret_cast<const float4*>(src[s] + 4 * qd);
-        *reinterpret_cast<float4*>(xs + (long long)s * xstride + 4 * x_quad_phys(EPL, qd)) = v;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qd < iq) v = *reinterpret_cast<const float4*>(src[s] + 4 * qd);
+        const int q = qd / QPC, j = qd - q * QPC;
+        const int phys = ((q >> 5) * QPC + j) * 32 + (q & 31);
+        *reinterpret_cast<float4*>(xs + (long long)s * xstride + 4 * phys) = v;
     }
 }
+
+__host__ __device__ constexpr int ilog2(int v) { int l = 0; while ((1 << l) < v) l++; return l; }
 
 // ---------------------------------------------------------------------------
 // Transposed warp reduction of V (power of two, <= 32) values: afterwards lane
@@ -510,7 +529,7 @@ __device__ __forceinline__ float lds_f32(uint32_t a)
 }
 
 // ---------------------------------------------------------------------------
-// mbarriers and bulk (TMA engine) copies.  Every wait is bounded in time: a
+// mbarriers and tensor (TMA engine) copies.  Every wait is bounded in time: a
 // wait that has not completed after kWaitNs returns false and the caller
 // records QSTATUS_DEVICE_TIMEOUT and leaves.
 // ---------------------------------------------------------------------------
@@ -551,17 +570,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitNs) return false;
-    return true;
+    for (uint32_t n = 1;; n++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) == 0 && global_ns() - t0 > kWaitNs) return false;   // the clock every 16 tries
+    }
 }
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
-// from global memory into this CTA's shared memory; completion is counted on
-// mbarrier `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+// Every thread of the CTA arrives on `bar` (initialized for all of them) and
+// waits for the others; `parity` tracks the barrier's phase.  False after
+// kWaitNs.
+__device__ __forceinline__ bool cta_barrier(uint32_t bar, uint32_t& parity)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+    mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, parity);
+    parity ^= 1u;
+    return ok;
+}
+// Tensor copy of one 2-D box (inner coordinate c0 in 4-byte elements, row
+// coordinate c1) of the tensor map at `map` into this CTA's shared memory at
+// `dst`; completion is counted on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int c0, int c1, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
 }
 
 // Bytes of one ring slot: NR chunk rows x 32 lanes (16 B of codes, int3 also

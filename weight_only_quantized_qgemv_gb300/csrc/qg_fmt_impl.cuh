@@ -39,6 +39,20 @@ __host__ __device__ constexpr int rows_per_tile()
     return by_rows < by_acc ? by_rows : by_acc;
 }
 
+// Rows per tile of the tile kernel: up to QG_TILE_RMAX / NM rows of each
+// matrix, at most 8 accumulators (S x NM x R).
+#ifndef QG_TILE_RMAX
+#define QG_TILE_RMAX 4
+#endif
+template <int S, int NM>
+__host__ __device__ constexpr int tile_rows_per()
+{
+    constexpr int rmax = FMT == FMT_INT3_G64 ? (QG_TILE_RMAX < 4 ? QG_TILE_RMAX : 4) : QG_TILE_RMAX;
+    constexpr int by_acc = 8 / (S * NM) > 0 ? 8 / (S * NM) : 1;
+    constexpr int by_rows = rmax / NM > 0 ? rmax / NM : 1;
+    return by_rows < by_acc ? by_rows : by_acc;
+}
+
 #ifndef QG_RING
 #define QG_RING 3
 #endif
@@ -77,10 +91,19 @@ __host__ __device__ constexpr int ring_stride_bytes()
     return kRing * ring_slot_bytes<FMT, NM * rows_per_tile<S, NM>()>();
 }
 
+// Tensor-copy sources of the tile kernel: per matrix m, tm[3m] codes (int3:
+// plane A), tm[3m + 1] int3 plane B, tm[3m + 2] scales, each a tensor of rows;
+// row r of expert e of piece p is tensor row e * row_mul[p] + row_add[p] + r.
 template <int NM>
-struct DenseJob : RingLayout {
+struct TileSource {
+    TileLayout tile;
+    CUtensorMap tm[3 * NM];
+    long long row_mul[3], row_add[3];
+};
+
+template <int NM>
+struct DenseJob : RingLayout, TileSource<NM> {
     static constexpr bool kLoopS = false;     // activation rows share each decoded word
-    BulkLayout bulk;
     Mat m[NM];
     const float* x;      // [S][I]
     float* y;            // y[s * ldy + row]
@@ -100,13 +123,13 @@ struct DenseJob : RingLayout {
     __device__ void store(int, int s, long long row, float v) const { y[(long long)s * ldy + row] = v; }
     __device__ int width() const { return m[0].I; }
     __device__ int* status_word() const { return nullptr; }
+    __device__ long long expert_of(int) const { return 0; }
 };
 
 // Expert phase A: the gate and up rows of every used expert, against the
 // tokens routed to it; stores h = silu(g) * u per sorted pair.
-struct ExpertUpJob : RingLayout {
+struct ExpertUpJob : RingLayout, TileSource<2> {
     static constexpr bool kLoopS = true;      // one-pair tiles, one pass of arithmetic per pair
-    BulkLayout bulk;
     int* status;
     Mat gate0, up0;                 // expert 0's matrices (w, sc advanced per expert)
     long long mat_bytes, mat_scales;
@@ -138,13 +161,13 @@ struct ExpertUpJob : RingLayout {
     }
     __device__ int width() const { return D; }
     __device__ int* status_word() const { return status; }
+    __device__ long long expert_of(int b) const { return batches[b].x; }
 };
 
 // Expert phase B: the down rows of every used expert against the h vectors of
 // its pairs; stores z = down h per sorted pair.
-struct ExpertDownJob : RingLayout {
+struct ExpertDownJob : RingLayout, TileSource<1> {
     static constexpr bool kLoopS = true;
-    BulkLayout bulk;
     int* status;
     Mat down0;
     long long mat_bytes, mat_scales;
@@ -172,6 +195,7 @@ struct ExpertDownJob : RingLayout {
     }
     __device__ int width() const { return F; }
     __device__ int* status_word() const { return status; }
+    __device__ long long expert_of(int b) const { return batches[b].x; }
 };
 
 // Hands finished tiles to the job (NM = 2: h = silu(gate) * up).  A reduced
@@ -259,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     }
 }
 
-#include "qg_bulk.cuh"
+#include "qg_tile.cuh"
 
 // ---------------------------------------------------------------------------
 // Dequantization: one thread per chunk, the same decoding arithmetic as the
@@ -348,93 +372,120 @@ static cudaError_t set_smem(K kernel, size_t bytes, int (&granted)[64])
     return e;
 }
 
-#ifndef QG_BULK
-#define QG_BULK 0
+#ifndef QG_TILE
+#define QG_TILE 1
+#endif
+#ifndef QG_TILE_PMAX
+#define QG_TILE_PMAX 8
 #endif
 
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Plans the bulk-copy kernel for rows of I inputs, NM matrices per tile, R
-// rows per tile and x_bytes of activation rows.  False when the shapes do not
-// allow it (scale rows or int3 plane-B rows not a multiple of 16 bytes) or
-// fewer than two stages fit; the per-lane copy kernel then runs instead.
-#ifndef QG_BULK_STAGE
-#define QG_BULK_STAGE 65536
-#endif
-#ifndef QG_BULK_NSTAGE
-#define QG_BULK_NSTAGE 4
-#endif
-static bool plan_bulk(int NM, int R, int I, int gs, size_t x_bytes, BulkLayout& L)
+// Plans the tile kernel's shared memory for NM matrices, R rows per tile, rows
+// of I inputs in groups of gs and xrows staged activation rows.  False when
+// the shapes do not suit it (a slice's scales under 16 bytes) or fewer than
+// two slots per warp fit; the per-warp ring kernel then runs instead.
+static bool plan_tile(int NM, int R, int I, int gs, int xrows, TileLayout& L)
 {
-    if (!QG_BULK) return false;
-    L.rb = FMT == FMT_INT8_ROW ? I : (FMT == FMT_INT3_G64 ? I / 4 : I / 2);
-    L.rbB = FMT == FMT_INT3_G64 ? I / 8 : 0;
-    L.sb = FMT == FMT_INT8_ROW ? 0 : (I / gs) * 4;
-    if (L.rb % 16 || L.rbB % 16 || L.sb % 16) return false;
-    const int nchunks = I / EPL;
-    const int nsteps = (nchunks + 31) / 32;
-    L.kp = (nsteps + 3) / 4;
-    L.kpw = (nsteps + L.kp - 1) / L.kp;
-    L.kp = (nsteps + L.kpw - 1) / L.kpw;
-    const int row_bytes = NM * (L.rb + L.rbB + L.sb);
-    const int tile_bytes = R * row_bytes;
-    const int x_end = align_up((int)x_bytes, 128);
-    // Largest stage (up to QG_BULK_STAGE bytes) that leaves room for at
-    // least three stages, else two.
-    for (int min_ns = 3; min_ns >= 2; min_ns--) {
-        for (int tps = QG_BULK_STAGE / tile_bytes > 0 ? QG_BULK_STAGE / tile_bytes : 1; tps >= 1; tps--) {
-            L.rs = tps * R;
-            L.stage_bytes = align_up(L.rs * row_bytes, 128);
-            L.stage_off = x_end;
-            for (int ns = QG_BULK_NSTAGE; ns >= min_ns; ns--) {
-                L.nstage = ns;
-                L.part_off = L.stage_off + ns * L.stage_bytes;
-                L.cnt_off = L.part_off + ns * tps * L.kp * 32 * 4;
-                L.bar_off = align_up(L.cnt_off + ns * tps * 4, 8);
-                L.total = L.bar_off + (2 * ns + 1) * 8;
-                if (L.total <= kSmemMax) {
-                    int off = 0;
-                    for (int m = 0; m < NM; m++) { L.w_off[m] = off; off += L.rs * L.rb; }
-                    for (int m = 0; m < NM; m++) { L.b_off[m] = off; off += L.rs * L.rbB; }
-                    for (int m = 0; m < NM; m++) { L.s_off[m] = off; off += L.rs * L.sb; }
-                    for (int m = NM; m < 2; m++) L.w_off[m] = L.b_off[m] = L.s_off[m] = 0;
-                    return true;
-                }
-            }
-        }
-    }
-    return false;
+    if (!QG_TILE) return false;
+    constexpr int KS = 32 * EPL;
+    L.nslices = (I + KS - 1) / KS;
+    L.xstride = L.nslices * KS;
+    L.sbox = FMT == FMT_INT8_ROW ? 0 : (KS / gs) * 4;
+    if (FMT != FMT_INT8_ROW && (KS % gs != 0 || L.sbox < 16)) return false;
+    L.tx_bytes = NM * R * (512 + (FMT == FMT_INT3_G64 ? 256 : 0) + L.sbox);
+    int off = 0;
+    for (int m = 0; m < 2; m++) L.code_off[m] = L.b_off[m] = L.s_off[m] = 0;
+    for (int m = 0; m < NM; m++) { L.code_off[m] = off; off = align_up(off + R * 512, 128); }
+    if (FMT == FMT_INT3_G64)
+        for (int m = 0; m < NM; m++) { L.b_off[m] = off; off = align_up(off + R * 256, 128); }
+    if (FMT != FMT_INT8_ROW)
+        for (int m = 0; m < NM; m++) { L.s_off[m] = off; off = align_up(off + R * L.sbox, 128); }
+    L.slot_bytes = off;
+    L.ring_off = align_up(xrows * L.xstride * 4, 128);
+    const int per_p = kTileWarps * L.slot_bytes;
+    int P = (kSmemMax - L.ring_off - 8 * (kTileWarps * QG_TILE_PMAX + 1)) / per_p;
+    if (P > QG_TILE_PMAX) P = QG_TILE_PMAX;
+    if (P < 2) return false;
+    L.P = P;
+    L.bar_off = L.ring_off + P * per_p;
+    L.total = L.bar_off + 8 * (kTileWarps * P + 1);
+    return true;
 }
 
-template <class K>
-static cudaError_t set_smem_max(K kernel, int (&granted)[64])
+// Code-row bytes of a matrix with I inputs (int3: plane A).
+static long long code_row_bytes(int I) { return FMT == FMT_INT8_ROW ? I : (FMT == FMT_INT3_G64 ? I / 4 : I / 2); }
+
+// Tensor maps of NM matrices of E experts (E = 1: a plain matrix) of O rows
+// and I inputs each, matrix bytes mat_bytes apart, R rows per tile.
+template <int NM>
+static bool tile_sources(TileSource<NM>& src, const void* const (&w)[NM], const float* const (&sc)[NM], long long E,
+                         long long O, int I, int gs, long long mat_bytes, int R)
 {
-    return set_smem(kernel, (size_t)kSmemMax, granted);
+    const long long rb = code_row_bytes(I);
+    const long long rbB = I / 8;
+    const long long sb = (long long)(I / gs) * 4;
+    const long long total = E * mat_bytes;
+    if (E * O >= (1ll << 31) || total / rb >= (1ll << 31) || (FMT == FMT_INT3_G64 && total / rbB >= (1ll << 31)))
+        return false;     // tensor rows and tile indices are 32-bit in the kernel
+    if (E > 1 && (mat_bytes % rb || (FMT == FMT_INT3_G64 && mat_bytes % rbB))) return false;
+    for (int m = 0; m < NM; m++) {
+        if (!encode_rows_map(&src.tm[3 * m], w[m], total / rb, rb, 512, R, false)) return false;
+        if (FMT == FMT_INT3_G64 && !encode_rows_map(&src.tm[3 * m + 1], w[m], total / rbB, rbB, 256, R, false))
+            return false;
+        if (FMT != FMT_INT8_ROW &&
+            !encode_rows_map(&src.tm[3 * m + 2], sc[m], E * O, sb, src.tile.sbox, R, true))
+            return false;
+    }
+    src.row_mul[0] = mat_bytes / rb;
+    src.row_add[0] = 0;
+    src.row_mul[1] = FMT == FMT_INT3_G64 ? mat_bytes / rbB : 0;
+    src.row_add[1] = FMT == FMT_INT3_G64 ? 2 * O : 0;    // plane B follows O rows of plane A (2 O rows of I/8)
+    src.row_mul[2] = O;
+    src.row_add[2] = 0;
+    return true;
+}
+
+template <int NM, int S, class Job>
+static cudaError_t launch_tile(const Job& job, int grid, cudaStream_t st)
+{
+    auto kern = k_tile<NM, S, Job>;
+    static int granted[64];
+    cudaError_t e = set_smem(kern, (size_t)job.tile.total, granted);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kTileThreads, job.tile.total, st>>>(job);
+    return cudaGetLastError();
 }
 
 template <int NM, int S>
 static cudaError_t launch_dense(const DenseJob<NM>& job_in, int grid, size_t x_bytes, cudaStream_t st)
 {
     DenseJob<NM> job = job_in;
-    constexpr int R = rows_per_tile<S, NM>();
-    const int gs = FMT == FMT_INT8_ROW ? job.m[0].I : job.m[0].I / job.m[0].ngrp;
-    bool scales16 = true;
-    for (int k = 0; k < NM; k++) scales16 = scales16 && (reinterpret_cast<uintptr_t>(job.m[k].sc) & 15) == 0;
-    if (scales16 && plan_bulk(NM, R, job.m[0].I, gs, (size_t)S * job.m[0].I * sizeof(float), job.bulk)) {
-        auto kb = k_bulk<NM, S, DenseJob<NM>>;
-        static int granted_b[64];
-        cudaError_t e = set_smem_max(kb, granted_b);
-        if (e != cudaSuccess) return e;
-        kb<<<grid, (kBulkConsumers + 1) * 32, job.bulk.total, st>>>(job);
-        return cudaGetLastError();
+    constexpr int R = tile_rows_per<S, NM>();
+    const int I = job.m[0].I;
+    const int gs = FMT == FMT_INT8_ROW ? I : I / job.m[0].ngrp;
+    const void* w[NM];
+    const float* sc[NM];
+    for (int k = 0; k < NM; k++) {
+        w[k] = job.m[k].w;
+        sc[k] = job.m[k].sc;
     }
+    const long long O = job.m[0].O;
+    const long long mat_bytes = FMT == FMT_INT3_G64 ? O * (I / 4) + O * (I / 8) : O * code_row_bytes(I);
+    // Measured on GB300: with one activation row the int8/int4/MXFP4 rows are
+    // cheap to decode and the per-lane copy kernel is a little faster; int3
+    // and several activation rows go to the tile kernel.
+    const int policy = kernel_policy();
+    const bool prefer_tile = policy == QKERNEL_TILE || (policy == QKERNEL_AUTO && (S > 1 || FMT == FMT_INT3_G64));
+    if (prefer_tile && plan_tile(NM, R, I, gs, S, job.tile) &&
+        tile_sources<NM>(job, w, sc, 1, O, I, gs, mat_bytes, R))
+        return launch_tile<NM, S>(job, grid, st);
     auto kern = k_stream<NM, S, DenseJob<NM>>;
-    const int warps = kWarps;
-    const size_t smem = x_bytes + (size_t)warps * job.ring_stride;
+    const size_t smem = x_bytes + (size_t)kWarps * job.ring_stride;
     static int granted[64];
-    cudaError_t e = set_smem(kern, (size_t)x_bytes + (size_t)kWarps * job.ring_stride, granted);
+    cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
-    kern<<<grid, warps * 32, smem, st>>>(job);
+    kern<<<grid, kThreads, smem, st>>>(job);
     return cudaGetLastError();
 }
 
@@ -508,15 +559,14 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
     job.ring_off = (int)align16((size_t)a.smax * a.D * sizeof(float));
     job.ring_stride = ring_stride_bytes<2, 1>();
     job.status = a.status_dev;
-    const bool scales16 = ((reinterpret_cast<uintptr_t>(a.gate_s) | reinterpret_cast<uintptr_t>(a.up_s)) & 15) == 0;
-    if (scales16 &&
-        plan_bulk(2, rows_per_tile<1, 2>(), a.D, gs, (size_t)a.smax * a.D * sizeof(float), job.bulk)) {
-        auto kb = k_bulk<2, kExpertSmax, ExpertUpJob>;
-        static int granted_b[64];
-        cudaError_t e = set_smem_max(kb, granted_b);
-        if (e != cudaSuccess) return e;
-        kb<<<grid, (kBulkConsumers + 1) * 32, job.bulk.total, st>>>(job);
-        return cudaGetLastError();
+    {
+        const void* w[2] = {a.gate, a.up};
+        const float* sc[2] = {a.gate_s, a.up_s};
+        constexpr int R = tile_rows_per<1, 2>();
+        if (kernel_policy() != QKERNEL_RING && (long long)a.s * a.k * ((a.F + R - 1) / R) < (1ll << 31) &&
+            plan_tile(2, R, a.D, gs, a.smax, job.tile) &&
+            tile_sources<2>(job, w, sc, a.E, a.F, a.D, gs, job.mat_bytes, R))
+            return launch_tile<2, kExpertSmax>(job, grid, st);
     }
     auto kern = k_stream<2, kExpertSmax, ExpertUpJob>;
     const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
@@ -546,15 +596,14 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
     job.ring_off = (int)align16((size_t)a.smax * a.F * sizeof(float));
     job.ring_stride = ring_stride_bytes<1, 1>();
     job.status = a.status_dev;
-    const bool scales16 = (reinterpret_cast<uintptr_t>(a.down_s) & 15) == 0;
-    if (scales16 &&
-        plan_bulk(1, rows_per_tile<1, 1>(), a.F, gs, (size_t)a.smax * a.F * sizeof(float), job.bulk)) {
-        auto kb = k_bulk<1, kExpertSmax, ExpertDownJob>;
-        static int granted_b[64];
-        cudaError_t e = set_smem_max(kb, granted_b);
-        if (e != cudaSuccess) return e;
-        kb<<<grid, (kBulkConsumers + 1) * 32, job.bulk.total, st>>>(job);
-        return cudaGetLastError();
+    {
+        const void* w[1] = {a.down};
+        const float* sc[1] = {a.down_s};
+        constexpr int R = tile_rows_per<1, 1>();
+        if (kernel_policy() != QKERNEL_RING && (long long)a.s * a.k * ((a.D + R - 1) / R) < (1ll << 31) &&
+            plan_tile(1, R, a.F, gs, a.smax, job.tile) &&
+            tile_sources<1>(job, w, sc, a.E, a.D, a.F, gs, job.mat_bytes, R))
+            return launch_tile<1, kExpertSmax>(job, grid, st);
     }
     auto kern = k_stream<1, kExpertSmax, ExpertDownJob>;
     const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
@@ -568,10 +617,10 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
 int QG_CAT(device_error_, QG_NAME)(int clear)
 {
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_bulk_error, sizeof(int)) != cudaSuccess) return QSTATUS_LAUNCH;
+    if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(int)) != cudaSuccess) return QSTATUS_LAUNCH;
     if (clear && v) {
         const int zero = 0;
-        cudaMemcpyToSymbol(g_bulk_error, &zero, sizeof(int));
+        cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(int));
     }
     return v;
 }

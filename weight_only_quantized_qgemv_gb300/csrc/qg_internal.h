@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>            // CUtensorMap (the encoder is looked up at run time)
 #include <cuda_runtime.h>
 
 #include "qgemv.h"
@@ -15,10 +16,11 @@ namespace qg {
 #endif
 constexpr int kWarps = QG_WARPS;            // warps per CTA of the streaming kernels
 constexpr int kThreads = kWarps * 32;
-#ifndef QG_BULK_CONSUMERS
-#define QG_BULK_CONSUMERS 16
+#ifndef QG_TILE_WARPS
+#define QG_TILE_WARPS 16
 #endif
-constexpr int kBulkConsumers = QG_BULK_CONSUMERS;   // consumer warps of the bulk-copy kernels
+constexpr int kTileWarps = QG_TILE_WARPS;   // warps per CTA of the tile kernel
+constexpr int kTileThreads = kTileWarps * 32;
 constexpr int kSmax = 8;                    // activation rows per dense launch
 constexpr int kExpertSmax = 4;              // (token, rank) pairs per expert batch
 constexpr int kSmemMax = 227 * 1024;        // dynamic shared memory per CTA (sm_103a)
@@ -76,17 +78,31 @@ struct ExpertArgs {
     int smax;          // pairs per batch
 };
 
-// Shared-memory plan of a bulk-copy launch (byte offsets from the start of
-// dynamic shared memory; the activation rows sit at offset 0).
-struct BulkLayout {
-    int rs;            // rows per stage
-    int nstage;        // stages in the ring
-    int kp;            // work units per row tile (K parts)
-    int kpw;           // warp steps per work unit
-    int stage_off, stage_bytes, part_off, cnt_off, bar_off, total;
-    int w_off[2], b_off[2], s_off[2];   // per matrix, inside a stage
-    int rb, rbB, sb;   // bytes per row: codes (int3: plane A), int3 plane B, scales (0: read from global)
+// Shared-memory plan of a tile-streaming launch (byte offsets from the start
+// of dynamic shared memory).  The activation rows sit at offset 0, zero-padded
+// to whole slices; then one ring of P slots per warp; then the mbarriers.
+// A slot holds one slice (32 lanes x EPL inputs) of R rows of every matrix:
+// their codes (512 B per row), int3 plane B (256 B per row) and scales
+// (sbox bytes per row).
+struct TileLayout {
+    int P;             // slots per warp ring
+    int slot_bytes;    // slot stride
+    int tx_bytes;      // bytes the tensor copies of one slot deliver
+    int ring_off;      // first ring
+    int bar_off;       // P full barriers per warp, then the CTA barrier
+    int total;         // dynamic shared memory of the launch
+    int nslices;       // slices per row
+    int xstride;       // floats per staged activation row (nslices * slice)
+    int sbox;          // scale bytes per row per slice
+    int code_off[2], b_off[2], s_off[2];   // per matrix, inside a slot
 };
+
+// Tensor map over `rows` rows of `row_bytes` bytes (a multiple of 16) at
+// `base` (16-byte aligned), read in boxes of `box_rows` rows x `box_bytes`
+// bytes (a multiple of 16, at most 1024): 32-bit elements, no swizzle,
+// out-of-range elements read as zero.  False when the driver refuses it.
+bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long long row_bytes, int box_bytes,
+                     int box_rows, bool f32);
 
 // Per-format launchers (defined in qg_fmt_<format>.cu).  Each returns a
 // cudaError_t of the launch.
@@ -107,6 +123,9 @@ QG_DECLARE_FMT(int3)
 QG_DECLARE_FMT(mxfp4)
 
 #undef QG_DECLARE_FMT
+
+// The process's QKERNEL_* policy (qg_abi.cu).
+int kernel_policy();
 
 // Format-independent expert kernels (qg_abi.cu).
 cudaError_t expert_prep(const ExpertArgs& a, cudaStream_t st);
