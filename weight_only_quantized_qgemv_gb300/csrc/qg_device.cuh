@@ -63,6 +63,14 @@ __device__ __forceinline__ int x_quad_phys(int EPL, int qd)
 // ---------------------------------------------------------------------------
 // Packed f32x2 helpers (sm_100+ PTX).
 // ---------------------------------------------------------------------------
+#ifndef QG_F32X2_BUILTIN
+#define QG_F32X2_BUILTIN 0
+#endif
+#if QG_F32X2_BUILTIN
+// The compiler's own packed builtins: it sees the pairs and places them.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+#else
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
 {
     float2 d;
@@ -84,6 +92,7 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
+#endif
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
@@ -141,6 +150,10 @@ __device__ __forceinline__ void load_chunk(const Mat& m, long long o, int q, Chu
         sc = ldg_f32(m.sc + o * m.ngrp + (q >> m.gsh));
     }
 }
+
+#ifndef QG_INT3_SPREAD
+#define QG_INT3_SPREAD 1
+#endif
 
 #ifndef QG_CXX_LDS
 #define QG_CXX_LDS 1
@@ -263,6 +276,45 @@ __device__ __forceinline__ void decode_int3_quad(const uint32_t (&c)[4], int m, 
     d[1] = fadd2(make_float2(u2f(__byte_perm(c[2], kMag0, sel)), u2f(__byte_perm(c[3], kMag0, sel))), B);
 }
 
+// int3, nibble form: the 16 elements 16j..16j+15 (plane A word A, plane B
+// bits in bytes sel of B) become two words of eight clean 3-bit codes, one per
+// nibble: ce holds the even elements (nibble k = element 16j + 2k), co the odd
+// ones.  Plane B's bit e is spread to bit 2e (byte permute, then three
+// shift-and-mask steps), which puts the high bit of element 2k at bit 4k + 2
+// after a shift by two and that of element 2k + 1 at bit 4k + 2 directly.
+template <uint32_t SEL>
+__device__ __forceinline__ void int3_nibbles(uint32_t A, uint32_t B, uint32_t& ce, uint32_t& co)
+{
+    uint32_t t = __byte_perm(B, 0u, SEL);              // the two plane-B bytes at bits 0..7 and 16..23
+    t = (t | (t << 4)) & 0x0F0F0F0Fu;
+    t = (t | (t << 2)) & 0x33333333u;
+    t = (t | (t << 1)) & 0x55555555u;                  // bit e of the 16 -> bit 2e
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, 0x33333333, 0xE4;" : "=r"(d) : "r"(A), "r"(t << 2));      // (a & m) | (b & ~m)
+    ce = d;
+    asm("lop3.b32 %0, %1, %2, 0x33333333, 0xE4;" : "=r"(d) : "r"(A >> 2), "r"(t));
+    co = d;
+}
+
+// Elements 16j + 2k and 16j + 2k + 1 (k = 0..3 from the low halves of ce and
+// co, k = 4..7 from the high halves) -> value pairs (code - 4).
+__device__ __forceinline__ void decode_int3_pairs(uint32_t ce, uint32_t co, float2 (&d)[8])
+{
+    const float2 B0 = make_float2(-8388612.0f, -8388612.0f);   // -(2^23 + 4)
+    const float2 B1 = make_float2(-524292.0f, -524292.0f);     // -(2^19 + 4)
+    const float2 B2 = make_float2(-32772.0f, -32772.0f);       // -(2^15 + 4)
+    const float2 B3 = make_float2(-2052.0f, -2052.0f);         // -(2^11 + 4)
+    const uint32_t he = ce >> 16, ho = co >> 16;
+    d[0] = fadd2(make_float2(u2f(and_or<0x000Fu>(ce, kMag0)), u2f(and_or<0x000Fu>(co, kMag0))), B0);
+    d[1] = fadd2(make_float2(u2f(and_or<0x00F0u>(ce, kMag1)), u2f(and_or<0x00F0u>(co, kMag1))), B1);
+    d[2] = fadd2(make_float2(u2f(and_or<0x0F00u>(ce, kMag2)), u2f(and_or<0x0F00u>(co, kMag2))), B2);
+    d[3] = fadd2(make_float2(u2f(and_or<0xF000u>(ce, kMag3)), u2f(and_or<0xF000u>(co, kMag3))), B3);
+    d[4] = fadd2(make_float2(u2f(and_or<0x000Fu>(he, kMag0)), u2f(and_or<0x000Fu>(ho, kMag0))), B0);
+    d[5] = fadd2(make_float2(u2f(and_or<0x00F0u>(he, kMag1)), u2f(and_or<0x00F0u>(ho, kMag1))), B1);
+    d[6] = fadd2(make_float2(u2f(and_or<0x0F00u>(he, kMag2)), u2f(and_or<0x0F00u>(ho, kMag2))), B2);
+    d[7] = fadd2(make_float2(u2f(and_or<0xF000u>(he, kMag3)), u2f(and_or<0xF000u>(ho, kMag3))), B3);
+}
+
 __device__ __forceinline__ uint32_t word(const uint4& v, int j)
 {
     return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
@@ -357,6 +409,33 @@ __device__ __forceinline__ void consume(const Chunk<FMT> (&c)[NR], const float (
                 for (int rr = 0; rr < NR; rr++) {
                     part[rr][s] = ffma2(d[rr][0], make_float2(xa.x, xa.y), part[rr][s]);
                     part[rr][s] = ffma2(d[rr][1], make_float2(xa.z, xa.w), part[rr][s]);
+                }
+            }
+        }
+    } else if constexpr (QG_INT3_SPREAD) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            float2 d[NR][8];
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) {
+                uint32_t ce, co;
+                const uint32_t B = (j & 2) ? c[rr].b.y : c[rr].b.x;
+                if (j & 1) int3_nibbles<0x4342u>(word(c[rr].a, j), B, ce, co);
+                else int3_nibbles<0x4140u>(word(c[rr].a, j), B, ce, co);
+                decode_int3_pairs(ce, co, d[rr]);
+            }
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                const int qd = 4 * j + m;
+#pragma unroll
+                for (int s = 0; s < S; s++) {
+                    if (s >= s_act) break;
+                    const float4 xv = lds4s(x_quad<PERM>(xq[s], xo, qd));
+#pragma unroll
+                    for (int rr = 0; rr < NR; rr++) {
+                        part[rr][s] = ffma2(d[rr][2 * m], make_float2(xv.x, xv.y), part[rr][s]);
+                        part[rr][s] = ffma2(d[rr][2 * m + 1], make_float2(xv.z, xv.w), part[rr][s]);
+                    }
                 }
             }
         }
