@@ -102,10 +102,15 @@ static int rows_per_launch(int fmt, int nm, int I)
 // Expert group: (token, rank) pairs sorted by (expert, pair index), split into
 // batches of at most smax pairs of one expert.
 // ---------------------------------------------------------------------------
+// It also splits the row tiles of each streaming phase over the G CTAs by
+// cost: a row tile of a batch of n pairs costs n (one pass of arithmetic per
+// pair), and CTA c starts at the tile where the cost so far reaches
+// total * c / G.  Tiles stay in order, so results do not change.
 __global__ void __launch_bounds__(1024) k_expert_prep(const int32_t* __restrict__ ids, int P, int k, int E, int smax,
-                                                      unsigned char* ws, WsLayout L, int32_t* status_dev)
+                                                      int G, int tpb_up, int tpb_down, unsigned char* ws,
+                                                      WsLayout L, int32_t* status_dev)
 {
-    __shared__ int s_ids[kMaxPairs];
+    __shared__ int s_ids[kMaxPairs + 1];
     __shared__ int s_sorted[kMaxPairs];
     __shared__ int s_bad;
     int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
@@ -141,19 +146,46 @@ __global__ void __launch_bounds__(1024) k_expert_prep(const int32_t* __restrict_
         pair_of[p] = pos;
     }
     __syncthreads();
+    __shared__ int s_nb;
     if (threadIdx.x == 0) {
         int nb = 0;
         for (int pos = 0; pos < P;) {
             const int e = s_sorted[pos];
             int n = 1;
             while (pos + n < P && s_sorted[pos + n] == e && n < smax) n++;
-            batches[nb++] = make_int4(e, pos, n, 0);
+            batches[nb] = make_int4(e, pos, n, 0);
+            s_ids[nb] = pos;                       // pairs before batch nb (ids are no longer needed)
+            nb++;
             pos += n;
         }
+        s_ids[nb] = P;
+        s_nb = nb;
         hdr[0] = QSTATUS_OK;
         hdr[1] = nb;
         hdr[2] = P;
         if (status_dev) *status_dev = QSTATUS_OK;
+    }
+    __syncthreads();
+    const int nb = s_nb;
+    int32_t* bounds = reinterpret_cast<int32_t*>(ws + L.bounds);
+    for (int i = threadIdx.x; i < 2 * (G + 1); i += blockDim.x) {
+        const int phase = i / (G + 1), c = i - phase * (G + 1);
+        const long long tpb = phase ? tpb_down : tpb_up;
+        long long tile = (long long)nb * tpb;
+        if (c < G && tpb > 0) {
+            const long long x = (long long)P * tpb * c / G;     // cost before CTA c
+            int lo = 0, hi = nb - 1;                            // last batch starting at or before x
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if ((long long)s_ids[mid] * tpb <= x) lo = mid;
+                else hi = mid - 1;
+            }
+            const long long n = s_ids[lo + 1] - s_ids[lo];
+            tile = (long long)lo * tpb + (x - (long long)s_ids[lo] * tpb) / n;
+        } else if (c < G) {
+            tile = 0;
+        }
+        bounds[phase * (kMaxGrid + 1) + c] = (int32_t)tile;   // the layout's two rows of kMaxGrid + 1
     }
 }
 
@@ -178,7 +210,8 @@ __global__ void k_expert_combine(const float* __restrict__ wts, int k, int D, co
 cudaError_t expert_prep(const ExpertArgs& a, cudaStream_t st)
 {
     const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
-    k_expert_prep<<<1, 1024, 0, st>>>(a.ids, a.s * a.k, a.k, a.E, a.smax, a.ws, L, a.status_dev);
+    k_expert_prep<<<1, 1024, 0, st>>>(a.ids, a.s * a.k, a.k, a.E, a.smax, a.grid, a.tpb_up, a.tpb_down, a.ws, L,
+                                      a.status_dev);
     return cudaGetLastError();
 }
 
@@ -352,10 +385,21 @@ int qexpert_group(int fmt, int gs, const void* gate, const float* gate_s, const 
         return QSTATUS_MISALIGNED;
     if (ws_bytes < ws_layout(D, F, s, k).total) return QSTATUS_WORKSPACE;
     int status = QSTATUS_OK;
-    const int grid = sm_count(&status);
+    int grid = sm_count(&status);
     if (status) return status;
+    if (grid > kMaxGrid) grid = kMaxGrid;
 
     ExpertArgs a;
+    a.grid = grid;
+    int r_up = 1, r_dn = 1;
+    switch (fmt) {
+    case QFMT_INT8_ROW: r_up = tile_rows_int8(2); r_dn = tile_rows_int8(1); break;
+    case QFMT_INT4_G: r_up = tile_rows_int4(2); r_dn = tile_rows_int4(1); break;
+    case QFMT_INT3_G64: r_up = tile_rows_int3(2); r_dn = tile_rows_int3(1); break;
+    default: r_up = tile_rows_mxfp4(2); r_dn = tile_rows_mxfp4(1); break;
+    }
+    a.tpb_up = (F + r_up - 1) / r_up;
+    a.tpb_down = (D + r_dn - 1) / r_dn;
     a.gs = fmt == QFMT_INT8_ROW ? 0 : g_up;
     a.gate = gate; a.up = up; a.down = down;
     a.gate_s = gate_s; a.up_s = up_s; a.down_s = down_s;

@@ -124,6 +124,12 @@ struct DenseJob : RingLayout, TileSource<NM> {
     __device__ int width() const { return m[0].I; }
     __device__ int* status_word() const { return nullptr; }
     __device__ long long expert_of(int) const { return 0; }
+    // row tiles [t0, t1) of CTA c of G (T tiles in all): an even split
+    __device__ void cta_tiles(int c, int G, long long T, int& t0, int& t1) const
+    {
+        t0 = (int)(T * c / G);
+        t1 = (int)(T * (c + 1) / G);
+    }
 };
 
 // Expert phase A: the gate and up rows of every used expert, against the
@@ -137,6 +143,7 @@ struct ExpertUpJob : RingLayout, TileSource<2> {
     const int32_t* hdr;
     const int4* batches;
     const int32_t* pair_tok;
+    const int32_t* bounds;          // CTA tile bounds of this phase (G + 1 entries)
     float* h;
     int D, F;
 
@@ -162,6 +169,14 @@ struct ExpertUpJob : RingLayout, TileSource<2> {
     __device__ int width() const { return D; }
     __device__ int* status_word() const { return status; }
     __device__ long long expert_of(int b) const { return batches[b].x; }
+    // row tiles [t0, t1) of CTA c: the cost-balanced split the prep kernel wrote
+    __device__ void cta_tiles(int c, int, long long T, int& t0, int& t1) const
+    {
+        t0 = bounds[c];
+        t1 = bounds[c + 1];
+        t0 = t0 < 0 ? 0 : (t0 > T ? (int)T : t0);         // never trust a workspace word with an index
+        t1 = t1 < t0 ? t0 : (t1 > T ? (int)T : t1);
+    }
 };
 
 // Expert phase B: the down rows of every used expert against the h vectors of
@@ -173,6 +188,7 @@ struct ExpertDownJob : RingLayout, TileSource<1> {
     long long mat_bytes, mat_scales;
     const int32_t* hdr;
     const int4* batches;
+    const int32_t* bounds;
     const float* h;
     float* z;
     int D, F;
@@ -196,6 +212,14 @@ struct ExpertDownJob : RingLayout, TileSource<1> {
     __device__ int width() const { return F; }
     __device__ int* status_word() const { return status; }
     __device__ long long expert_of(int b) const { return batches[b].x; }
+    // row tiles [t0, t1) of CTA c: the cost-balanced split the prep kernel wrote
+    __device__ void cta_tiles(int c, int, long long T, int& t0, int& t1) const
+    {
+        t0 = bounds[c];
+        t1 = bounds[c + 1];
+        t0 = t0 < 0 ? 0 : (t0 > T ? (int)T : t0);         // never trust a workspace word with an index
+        t1 = t1 < t0 ? t0 : (t1 > T ? (int)T : t1);
+    }
 };
 
 // Hands finished tiles to the job (NM = 2: h = silu(gate) * up).  A reduced
@@ -554,6 +578,7 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
     job.batches = reinterpret_cast<const int4*>(a.ws + L.batches);
     job.pair_tok = reinterpret_cast<const int32_t*>(a.ws + L.pair_tok);
     job.h = reinterpret_cast<float*>(a.ws + L.h);
+    job.bounds = reinterpret_cast<const int32_t*>(a.ws + L.bounds);
     job.D = a.D;
     job.F = a.F;
     job.ring_off = (int)align16((size_t)a.smax * a.D * sizeof(float));
@@ -591,6 +616,7 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
     job.batches = reinterpret_cast<const int4*>(a.ws + L.batches);
     job.h = reinterpret_cast<const float*>(a.ws + L.h);
     job.z = reinterpret_cast<float*>(a.ws + L.z);
+    job.bounds = reinterpret_cast<const int32_t*>(a.ws + L.bounds) + (kMaxGrid + 1);
     job.D = a.D;
     job.F = a.F;
     job.ring_off = (int)align16((size_t)a.smax * a.F * sizeof(float));
@@ -623,6 +649,11 @@ int QG_CAT(device_error_, QG_NAME)(int clear)
         cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(int));
     }
     return v;
+}
+
+int QG_CAT(tile_rows_, QG_NAME)(int nm)
+{
+    return nm == 2 ? tile_rows_per<1, 2>() : tile_rows_per<1, 1>();
 }
 
 size_t QG_CAT(ring_bytes_, QG_NAME)(int nm)

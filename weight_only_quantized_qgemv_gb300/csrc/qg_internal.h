@@ -40,10 +40,12 @@ struct HostMat {
 //   batches  int4[P]      (expert, first sorted pair, pairs in batch, 0)
 //   pair_tok int32[P]     token of the sorted pair
 //   pair_of  int32[P]     sorted position of pair t * k + r
+//   bounds   int32[2][kMaxGrid + 1]  first row tile of each CTA (gate/up, down)
 //   h        f32[P][F]    silu(gate x) * (up x) of each sorted pair
 //   z        f32[P][D]    down h of each sorted pair
+constexpr int kMaxGrid = 1024;              // CTAs of an expert launch
 struct WsLayout {
-    size_t hdr, batches, pair_tok, pair_of, h, z, total;
+    size_t hdr, batches, pair_tok, pair_of, bounds, h, z, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -58,6 +60,7 @@ inline WsLayout ws_layout(int D, int F, int s, int k)
     L.batches = off;  off = align256(off + P * 4 * sizeof(int32_t));
     L.pair_tok = off; off = align256(off + P * sizeof(int32_t));
     L.pair_of = off;  off = align256(off + P * sizeof(int32_t));
+    L.bounds = off;   off = align256(off + 2 * (kMaxGrid + 1) * sizeof(int32_t));
     L.h = off;        off = align256(off + P * (size_t)F * sizeof(float));
     L.z = off;        off = align256(off + P * (size_t)D * sizeof(float));
     L.total = off;
@@ -76,6 +79,8 @@ struct ExpertArgs {
     unsigned char* ws;
     int32_t* status_dev;
     int smax;          // pairs per batch
+    int grid;               // CTAs of the streaming launches (<= kMaxGrid)
+    int tpb_up, tpb_down;   // row tiles per batch of the tile kernel's two phases
 };
 
 // Shared-memory plan of a tile-streaming launch (byte offsets from the start
@@ -115,6 +120,7 @@ bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long lo
     cudaError_t expert_down_##name(const ExpertArgs& a, int grid, cudaStream_t st);                     \
     cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);                         \
     size_t ring_bytes_##name(int nm);                                                                 \
+    int tile_rows_##name(int nm);                                                                     \
     int device_error_##name(int clear);
 
 QG_DECLARE_FMT(int8)

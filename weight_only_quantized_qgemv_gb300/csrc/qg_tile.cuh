@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
 
     const int tpb = (int)((job.rows_per() + R - 1) / R);    // tiles per batch
     const long long T = (long long)job.nbatch() * tpb;
-    const int t0 = (int)(T * blockIdx.x / gridDim.x);
-    const int t1 = (int)(T * (blockIdx.x + 1) / gridDim.x);
+    int t0, t1;
+    job.cta_tiles(blockIdx.x, gridDim.x, T, t0, t1);
     if (t0 >= t1) return;
 
     // ---- producer: lane 0 issues, every lane keeps the same state ----
