@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(1024) k_expert_prep(const int32_t* __restrict_
     __shared__ int s_ids[kMaxPairs + 1];
     __shared__ int s_sorted[kMaxPairs];
     __shared__ int s_bad;
+    pdl_wait_prev();              // ids may come from the kernel before; the workspace may still be read
+    pdl_allow_next();
     int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
     int4* batches = reinterpret_cast<int4*>(ws + L.batches);
     int32_t* pair_tok = reinterpret_cast<int32_t*>(ws + L.pair_tok);
@@ -193,6 +195,8 @@ __global__ void __launch_bounds__(1024) k_expert_prep(const int32_t* __restrict_
 __global__ void k_expert_combine(const float* __restrict__ wts, int k, int D, const unsigned char* ws, WsLayout L,
                                  float* __restrict__ out)
 {
+    pdl_allow_next();
+    pdl_wait_prev();              // z comes from the down phase
     const int t = blockIdx.y;
     const int d = blockIdx.x * blockDim.x + threadIdx.x;
     if (d >= D) return;
@@ -210,17 +214,16 @@ __global__ void k_expert_combine(const float* __restrict__ wts, int k, int D, co
 cudaError_t expert_prep(const ExpertArgs& a, cudaStream_t st)
 {
     const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
-    k_expert_prep<<<1, 1024, 0, st>>>(a.ids, a.s * a.k, a.k, a.E, a.smax, a.grid, a.tpb_up, a.tpb_down, a.ws, L,
-                                      a.status_dev);
-    return cudaGetLastError();
+    return launch_pdl(k_expert_prep, dim3(1), dim3(1024), 0, st, a.ids, a.s * a.k, a.k, a.E, a.smax, a.grid,
+                      a.tpb_up, a.tpb_down, a.ws, L, a.status_dev);
 }
 
 cudaError_t expert_combine(const ExpertArgs& a, cudaStream_t st)
 {
     const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
     dim3 grid((a.D + 255) / 256, a.s);
-    k_expert_combine<<<grid, 256, 0, st>>>(a.wts, a.k, a.D, a.ws, L, a.out);
-    return cudaGetLastError();
+    return launch_pdl(k_expert_combine, grid, dim3(256), 0, st, a.wts, a.k, a.D,
+                      static_cast<const unsigned char*>(a.ws), L, a.out);
 }
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link against

@@ -104,6 +104,9 @@ struct TileSource {
 template <int NM>
 struct DenseJob : RingLayout, TileSource<NM> {
     static constexpr bool kLoopS = false;     // activation rows share each decoded word
+    // Reads nothing the previous kernel may write before the activations: the
+    // weight stream may start before that kernel completes.
+    static constexpr bool kWaitFirst = false;
     Mat m[NM];
     const float* x;      // [S][I]
     float* y;            // y[s * ldy + row]
@@ -136,6 +139,10 @@ struct DenseJob : RingLayout, TileSource<NM> {
 // tokens routed to it; stores h = silu(g) * u per sorted pair.
 struct ExpertUpJob : RingLayout, TileSource<2> {
     static constexpr bool kLoopS = true;      // one-pair tiles, one pass of arithmetic per pair
+    // Its batches come from the prep kernel just before it: wait first.  (It
+    // lets the down phase start only after that, so the down phase may read
+    // the batches early.)
+    static constexpr bool kWaitFirst = true;
     int* status;
     Mat gate0, up0;                 // expert 0's matrices (w, sc advanced per expert)
     long long mat_bytes, mat_scales;
@@ -183,6 +190,9 @@ struct ExpertUpJob : RingLayout, TileSource<2> {
 // its pairs; stores z = down h per sorted pair.
 struct ExpertDownJob : RingLayout, TileSource<1> {
     static constexpr bool kLoopS = true;
+    // The batches were complete before the up phase let this kernel start;
+    // only h (the up phase's output) needs the wait.
+    static constexpr bool kWaitFirst = false;
     int* status;
     Mat down0;
     long long mat_bytes, mat_scales;
@@ -266,6 +276,7 @@ __device__ __forceinline__ void segment(const Job& job, int b, long long l0, lon
              (uint32_t)(job.ring_off + warp * job.ring_stride));   // copies in flight during staging
     const int I = m[0].I;
     if (b != staged) {
+        if (!Job::kWaitFirst && staged < 0) pdl_wait_prev();   // before the first read of activations
         __syncthreads();
         const float* src[S];
 #pragma unroll
@@ -290,6 +301,8 @@ template <int NM, int S, class Job>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ Job job)
 {
     float* xs = reinterpret_cast<float*>(qg_smem4);
+    if constexpr (Job::kWaitFirst) pdl_wait_prev();
+    pdl_allow_next();
     if (job.bad()) return;
     const long long rows_per = job.rows_per();
     const long long N = (long long)job.nbatch() * rows_per;
@@ -477,8 +490,7 @@ static cudaError_t launch_tile(const Job& job, int grid, cudaStream_t st)
     static int granted[64];
     cudaError_t e = set_smem(kern, (size_t)job.tile.total, granted);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kTileThreads, job.tile.total, st>>>(job);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kTileThreads), (size_t)job.tile.total, st, job);
 }
 
 template <int NM, int S>
@@ -509,8 +521,7 @@ static cudaError_t launch_dense(const DenseJob<NM>& job_in, int grid, size_t x_b
     static int granted[64];
     cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(job);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
 }
 
 template <int NM>
@@ -598,8 +609,7 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
     static int granted[64];
     cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(job);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
 }
 
 cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st)
@@ -636,8 +646,7 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
     static int granted[64];
     cudaError_t e = set_smem(kern, smem, granted);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(job);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
 }
 
 int QG_CAT(device_error_, QG_NAME)(int clear)

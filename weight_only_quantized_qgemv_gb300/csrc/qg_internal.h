@@ -133,6 +133,35 @@ QG_DECLARE_FMT(mxfp4)
 // The process's QKERNEL_* policy (qg_abi.cu).
 int kernel_policy();
 
+// Launches allowing programmatic dependent launch: the kernel may start while
+// the previous kernel in the stream finishes, if that one lets it (each of
+// this library's kernels does, early); the kernel itself waits for the
+// previous one before it touches anything the previous one may write.
+#ifndef QG_PDL
+#define QG_PDL 1
+#endif
+// Device side: let the next kernel in the stream start (it waits for this one
+// before touching what this one writes), and wait for the previous kernel to
+// complete with its memory visible.
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = QG_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Format-independent expert kernels (qg_abi.cu).
 cudaError_t expert_prep(const ExpertArgs& a, cudaStream_t st);
 cudaError_t expert_combine(const ExpertArgs& a, cudaStream_t st);

@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
     float* xs = reinterpret_cast<float*>(qg_smem4);
     int* status = job.status_word();
 
+    if constexpr (Job::kWaitFirst) pdl_wait_prev();
+    pdl_allow_next();
     if (job.bad()) return;
     if (sbase & 127u) {                           // tensor copies land on 128-byte boundaries
         if (threadIdx.x == 0) tile_fail(status);
@@ -175,6 +177,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
         const int s_act = job.batch_S(b);
         // stage the batch's activation rows (after everyone is done with the last)
         if (seg0 != t0 && !cta_barrier(ctabar, cta_phase)) { ok = false; break; }
+        if (!Job::kWaitFirst && seg0 == t0) pdl_wait_prev();   // before the first read of activations
         {
             const float* src[S];
 #pragma unroll
