@@ -26,6 +26,12 @@
  *  - Calls are asynchronous on the given CUDA stream (`stream` is a
  *    cudaStream_t; NULL is the legacy default stream).  They return once the
  *    work is enqueued; the caller synchronizes before reading results.
+ *  - Kernels are launched with programmatic dependent launch: when the kernel
+ *    before a call in the stream allows it (this library's kernels do), the
+ *    call starts reading its packed weights and scales before that kernel has
+ *    finished; activations, ids, router weights and the workspace are read,
+ *    and outputs written, only after it completed.  So weights and scales
+ *    must not be written by a kernel that allows early starts of the next.
  *  - Every call returns a status: QSTATUS_OK (0) or a negative code.  On a
  *    negative return nothing was enqueued, except QSTATUS_LAUNCH (a CUDA error
  *    at launch; qlast_cuda_error() has its text).  There is no CPU fallback.
