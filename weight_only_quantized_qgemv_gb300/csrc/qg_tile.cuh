@@ -260,17 +260,30 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
                 }
             }
             if (!ok) break;
-            float v[V];
+            constexpr int V1 = pow2_ceil(R * NM);        // one activation row in use (the common expert batch)
+            if (LOOP && V1 < V && s_act == 1) {
+                float v[V1];
 #pragma unroll
-            for (int i = 0; i < V; i++) v[i] = 0.f;
-#pragma unroll
-            for (int s = 0; s < S; s++)
+                for (int i = 0; i < V1; i++) v[i] = 0.f;
 #pragma unroll
                 for (int r = 0; r < R; r++)
 #pragma unroll
-                    for (int m = 0; m < NM; m++) v[(s * R + r) * NM + m] = acc[s][m * R + r];
-            const float red = warp_reduce_scatter<V>(v, lane);
-            sink.template put<V>(red, reduce_scatter_index<V>(lane), lane < V, row0, rows);
+                    for (int m = 0; m < NM; m++) v[r * NM + m] = acc[0][m * R + r];
+                const float red = warp_reduce_scatter<V1>(v, lane);
+                sink.template put<V1>(red, reduce_scatter_index<V1>(lane), lane < V1, row0, rows);
+            } else {
+                float v[V];
+#pragma unroll
+                for (int i = 0; i < V; i++) v[i] = 0.f;
+#pragma unroll
+                for (int s = 0; s < S; s++)
+#pragma unroll
+                    for (int r = 0; r < R; r++)
+#pragma unroll
+                        for (int m = 0; m < NM; m++) v[(s * R + r) * NM + m] = acc[s][m * R + r];
+                const float red = warp_reduce_scatter<V>(v, lane);
+                sink.template put<V>(red, reduce_scatter_index<V>(lane), lane < V, row0, rows);
+            }
         }
         seg0 = seg1;
         b++;
