@@ -52,8 +52,8 @@
  *  - Sizes: I % 16 == 0 (int8), I % gs == 0 (grouped formats), O, I, s >= 1.
  *    The activation rows of one launch share shared memory with the weight
  *    copy rings, so a row of I f32 must fit what the rings leave: I up to
- *    about 27,000 (int8, int4, MXFP4) or 35,000 (int3); longer rows return
- *    QSTATUS_BAD_DIM.
+ *    about 37,000 (int8, int4, MXFP4; qgate_up and qexpert_group too) or
+ *    43,000 (int3); longer rows return QSTATUS_BAD_DIM.
  */
 #ifndef QGEMV_GB300_H
 #define QGEMV_GB300_H

@@ -54,7 +54,7 @@ __host__ __device__ constexpr int tile_rows_per()
 }
 
 #ifndef QG_RING
-#define QG_RING 3
+#define QG_RING 2
 #endif
 constexpr int kRing = QG_RING;   // chunk-register ring depth
 
@@ -262,11 +262,11 @@ struct Sink {
 
 // One segment: rows [l0, l1) of batch b, all warps of the CTA, with the
 // batch's s_act <= S activation rows; warp w takes the row tiles w, w + W, ...
-template <int NM, int S, class Job>
+template <int NM, int S, class Job, int RF = 0>
 __device__ __forceinline__ void segment(const Job& job, int b, long long l0, long long l1, int s_act, float* xs,
                                         int& staged)
 {
-    constexpr int R = rows_per_tile<Job::kLoopS ? 1 : S, NM>();
+    constexpr int R = RF > 0 ? RF : rows_per_tile<Job::kLoopS ? 1 : S, NM>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Mat m[NM];
     job.mats(b, m);
@@ -296,8 +296,10 @@ __device__ __forceinline__ void segment(const Job& job, int b, long long l0, lon
 // job's batches laid end to end (N = batches * rows per batch), so every SM
 // gets the same number of weight rows; the range splits into segments where
 // the batch (and so the staged activation set) changes.  S is the number of
-// activation rows the code is built for; a batch may use fewer.
-template <int NM, int S, class Job>
+// activation rows the code is built for; a batch may use fewer.  RF > 0
+// forces RF rows per tile (single rows for matrices too short to give every
+// warp a tile of the default height).
+template <int NM, int S, class Job, int RF = 0>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ Job job)
 {
     float* xs = reinterpret_cast<float*>(qg_smem4);
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         const long long base = (long long)b * rows_per;
         const long long l0 = r - base;
         const long long l1 = (r_end - base) < rows_per ? (r_end - base) : rows_per;
-        segment<NM, S>(job, b, l0, l1, job.batch_S(b), xs, staged);
+        segment<NM, S, Job, RF>(job, b, l0, l1, job.batch_S(b), xs, staged);
         r = base + l1;
     }
 }
@@ -413,7 +415,7 @@ static cudaError_t set_smem(K kernel, size_t bytes, int (&granted)[64])
 #define QG_TILE 1
 #endif
 #ifndef QG_TILE_PMAX
-#define QG_TILE_PMAX 8
+#define QG_TILE_PMAX 3
 #endif
 
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -516,6 +518,18 @@ static cudaError_t launch_dense(const DenseJob<NM>& job_in, int grid, size_t x_b
     if (prefer_tile && plan_tile(NM, R, I, gs, S, job.tile) &&
         tile_sources<NM>(job, w, sc, 1, O, I, gs, mat_bytes, R))
         return launch_tile<NM, S>(job, grid, st);
+    if constexpr (S == 1) {
+        // fewer rows per CTA than warps x tile height: single-row tiles keep more warps busy
+        if ((O + grid - 1) / grid < (long long)kWarps * rows_per_tile<1, NM>()) {
+            auto kern1 = k_stream<NM, 1, DenseJob<NM>, 1>;
+            job.ring_stride = kRing * ring_slot_bytes<FMT, NM>();
+            const size_t smem1 = x_bytes + (size_t)kWarps * job.ring_stride;
+            static int granted1[64];
+            cudaError_t e = set_smem(kern1, smem1, granted1);
+            if (e != cudaSuccess) return e;
+            return launch_pdl(kern1, dim3(grid), dim3(kThreads), smem1, st, job);
+        }
+    }
     auto kern = k_stream<NM, S, DenseJob<NM>>;
     const size_t smem = x_bytes + (size_t)kWarps * job.ring_stride;
     static int granted[64];
