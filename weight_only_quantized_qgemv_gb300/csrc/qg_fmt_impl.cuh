@@ -40,9 +40,10 @@ __host__ __device__ constexpr int rows_per_tile()
 }
 
 // Rows per tile of the tile kernel: up to QG_TILE_RMAX / NM rows of each
-// matrix, at most 8 accumulators (S x NM x R).
+// matrix, at most 8 accumulators (S x NM x R).  MXFP4 decodes with fewer live
+// registers and measured faster with taller tiles.
 #ifndef QG_TILE_RMAX
-#define QG_TILE_RMAX 4
+#define QG_TILE_RMAX (FMT == FMT_MXFP4_G32 ? 8 : 4)
 #endif
 template <int S, int NM>
 __host__ __device__ constexpr int tile_rows_per()
@@ -415,7 +416,7 @@ static cudaError_t set_smem(K kernel, size_t bytes, int (&granted)[64])
 #define QG_TILE 1
 #endif
 #ifndef QG_TILE_PMAX
-#define QG_TILE_PMAX 3
+#define QG_TILE_PMAX 2
 #endif
 
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
