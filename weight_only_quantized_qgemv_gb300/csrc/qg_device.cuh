@@ -500,7 +500,29 @@ __device__ __forceinline__ void stage_rows_perm(float* xs, int xstride, const fl
                                                 int t, int nthreads)
 {
     constexpr int QPC = EPL / 4;              // quads per chunk
-    const int nq = xstride / 4, iq = I / 4;
+    const int iq = I / 4;
+    if (nrows >= 2) {
+        // Several rows (measured faster with this order): one thread per chunk;
+        // it reads the chunk's contiguous quads and writes quad j where the warp
+        // step's 32 chunks sit side by side, so the 32 threads of a warp store
+        // consecutive float4 (no bank conflicts).
+        const int nc = xstride / EPL;
+        for (int idx = t; idx < nrows * nc; idx += nthreads) {
+            const int s = idx / nc;
+            const int q = idx - s * nc;
+            const float* src_q = src[s] + 4 * q * QPC;
+            float* dst = xs + (long long)s * xstride + 4 * ((q >> 5) * QPC * 32 + (q & 31));
+#pragma unroll 4
+            for (int j = 0; j < QPC; j++) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q * QPC + j < iq) v = *reinterpret_cast<const float4*>(src_q + 4 * j);
+                *reinterpret_cast<float4*>(dst + 4 * 32 * j) = v;
+            }
+        }
+        return;
+    }
+    // One row: one thread per quad (coalesced reads).
+    const int nq = xstride / 4;
     for (int idx = t; idx < nrows * nq; idx += nthreads) {
         const int s = idx / nq;
         const int qd = idx - s * nq;

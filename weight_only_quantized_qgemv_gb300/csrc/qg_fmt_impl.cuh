@@ -40,16 +40,21 @@ __host__ __device__ constexpr int rows_per_tile()
 }
 
 // Rows per tile of the tile kernel: up to QG_TILE_RMAX / NM rows of each
-// matrix, at most 8 accumulators (S x NM x R).  MXFP4 decodes with fewer live
+// matrix, at most 16 accumulators (S x NM x R), so that each x quad loaded
+// from shared memory serves four rows up to four activation rows (shared
+// memory bandwidth bounds the several-row case).  MXFP4 decodes with fewer live
 // registers and measured faster with taller tiles.
 #ifndef QG_TILE_RMAX
 #define QG_TILE_RMAX (FMT == FMT_MXFP4_G32 ? 8 : 4)
+#endif
+#ifndef QG_TILE_ACC
+#define QG_TILE_ACC 16
 #endif
 template <int S, int NM>
 __host__ __device__ constexpr int tile_rows_per()
 {
     constexpr int rmax = FMT == FMT_INT3_G64 ? (QG_TILE_RMAX < 4 ? QG_TILE_RMAX : 4) : QG_TILE_RMAX;
-    constexpr int by_acc = 8 / (S * NM) > 0 ? 8 / (S * NM) : 1;
+    constexpr int by_acc = QG_TILE_ACC / (S * NM) > 0 ? QG_TILE_ACC / (S * NM) : 1;
     constexpr int by_rows = rmax / NM > 0 ? rmax / NM : 1;
     return by_rows < by_acc ? by_rows : by_acc;
 }
