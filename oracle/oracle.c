@@ -34,8 +34,9 @@
  *    (bias 1), one mantissa bit; exponent 0 is subnormal (0 or 0.5).
  *  - Groups run along i inside a row: element (o, i) takes scale
  *    [o][i / gs], scales stored row-major [O][I/gs].  int8 per row: gs = I.
- *  - silu(z) = z / (1 + exp(-z)).
- *  - out[t] = sum over rank r of w[t][r] * down_e (silu(gate_e x_t) * up_e x_t)
+ *  - silu(z) = z / (1 + exp(-z)); the activation is silu(g) * u, or with a
+ *    limit L (clamped SwiGLU) silu(min(g, L)) * min(max(u, -L), L).
+ *  - out[t] = sum over rank r of w[t][r] * down_e (act(gate_e x_t, up_e x_t))
  *    with e = ids[t][r], summed in rank order.
  *
  * Everything is evaluated in double from the f32 inputs, in index order, with
@@ -185,19 +186,41 @@ double oracle_silu(double z)
     return z / (1.0 + exp(-z));
 }
 
+/* The gate/up activation.  act 0: silu(g) * u (SwiGLU).  act 1: SwiGLU with
+ * a limit L (the pages' swiglu_limit, [VULKAN] expert-tier paragraph on
+ * GLM-5.3 Flash): the gate is capped at L and the up value clamped to
+ * [-L, L] before the product, so that L = 0 zeroes the output (the page's
+ * swiglu_clamped "clamps at any limit, including 0"). */
+double oracle_glu(int act, double limit, double g, double u)
+{
+    if (act == 1) {
+        if (g > limit) g = limit;
+        if (u > limit) u = limit;
+        if (u < -limit) u = -limit;
+    }
+    return oracle_silu(g) * u;
+}
+
 /* Step a4 ([GUIDE] API contract, coli_vk_gate_up): h[t][f] = silu(g) * u with
  * g = gate[f] . x[t] and u = up[f] . x[t]; gate and up are F x D. */
-void oracle_qgate_up(int fmt, long gs, const uint8_t *wg, const float *sg,
-                     const uint8_t *wu, const float *su, const float *x,
-                     long F, long D, long s, double *h)
+void oracle_qgate_up_act(int fmt, long gs, const uint8_t *wg, const float *sg,
+                         const uint8_t *wu, const float *su, const float *x,
+                         long F, long D, long s, int act, double limit, double *h)
 {
 #pragma omp parallel for schedule(static)
     for (long f = 0; f < F; f++)
         for (long t = 0; t < s; t++) {
             double g = row_dot(fmt, gs, wg, sg, F, D, f, x + t * D);
             double u = row_dot(fmt, gs, wu, su, F, D, f, x + t * D);
-            h[t * F + f] = oracle_silu(g) * u;
+            h[t * F + f] = oracle_glu(act, limit, g, u);
         }
+}
+
+void oracle_qgate_up(int fmt, long gs, const uint8_t *wg, const float *sg,
+                     const uint8_t *wu, const float *su, const float *x,
+                     long F, long D, long s, double *h)
+{
+    oracle_qgate_up_act(fmt, gs, wg, sg, wu, su, x, F, D, s, 0, 0.0, h);
 }
 
 /* Step a4 on a sample of rows f = rows[j]. */
@@ -222,14 +245,14 @@ void oracle_qgate_up_rows(int fmt, long gs, const uint8_t *wg, const float *sg,
  *     out[t][d] += w[t][r] * (down_e[d] . h)      (rank order r = 0..k-1)
  * Only the output columns cols[0..ncols) are formed (all of them when
  * cols == NULL, then ncols must be D); out is double [s][ncols]. */
-void oracle_expert_group_cols(int fmt, long gs,
-                              const uint8_t *gate, const float *gate_s,
-                              const uint8_t *up, const float *up_s,
-                              const uint8_t *down, const float *down_s,
-                              long E, long D, long F,
-                              const float *x, long s, long k,
-                              const int32_t *ids, const float *wts,
-                              const long *cols, long ncols, double *out, double *h_scratch)
+void oracle_expert_group_act_cols(int fmt, long gs,
+                                  const uint8_t *gate, const float *gate_s,
+                                  const uint8_t *up, const float *up_s,
+                                  const uint8_t *down, const float *down_s,
+                                  long E, long D, long F,
+                                  const float *x, long s, long k,
+                                  const int32_t *ids, const float *wts, int act, double limit,
+                                  const long *cols, long ncols, double *out, double *h_scratch)
 {
     long gu_bytes = oracle_packed_bytes(fmt, F, D);
     long gu_scales = F * (D / group_of(fmt, D, gs));
@@ -252,7 +275,7 @@ void oracle_expert_group_cols(int fmt, long gs,
             for (long f = 0; f < F; f++) {
                 double g = row_dot(fmt, gs, ge, gse, F, D, f, x + t * D);
                 double u = row_dot(fmt, gs, ue, use, F, D, f, x + t * D);
-                h_scratch[f] = oracle_silu(g) * u;
+                h_scratch[f] = oracle_glu(act, limit, g, u);
             }
 #pragma omp parallel for schedule(static)
             for (long j = 0; j < ncols; j++) {
@@ -264,6 +287,20 @@ void oracle_expert_group_cols(int fmt, long gs,
             }
         }
     }
+}
+
+/* The same with SwiGLU (act 0). */
+void oracle_expert_group_cols(int fmt, long gs,
+                              const uint8_t *gate, const float *gate_s,
+                              const uint8_t *up, const float *up_s,
+                              const uint8_t *down, const float *down_s,
+                              long E, long D, long F,
+                              const float *x, long s, long k,
+                              const int32_t *ids, const float *wts,
+                              const long *cols, long ncols, double *out, double *h_scratch)
+{
+    oracle_expert_group_act_cols(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, 0,
+                                 0.0, cols, ncols, out, h_scratch);
 }
 
 /* Number of threads the OpenMP loops above use (1 when built without it). */

@@ -78,6 +78,11 @@ class Oracle:
         lib.oracle_qgemv_rows.argtypes = [I, L, P, P, P, L, L, L, P, L, P]
         lib.oracle_silu.argtypes = [D]
         lib.oracle_silu.restype = D
+        lib.oracle_glu.argtypes = [I, D, D, D]
+        lib.oracle_glu.restype = D
+        lib.oracle_qgate_up_act.argtypes = [I, L, P, P, P, P, P, L, L, L, I, D, P]
+        lib.oracle_expert_group_act_cols.argtypes = [I, L, P, P, P, P, P, P, L, L, L, P, L, L, P, P, I, D, P, L,
+                                                     P, P]
         lib.oracle_qgate_up.argtypes = [I, L, P, P, P, P, P, L, L, L, P]
         lib.oracle_qgate_up_rows.argtypes = [I, L, P, P, P, P, P, L, L, L, P, L, P]
         lib.oracle_expert_group_cols.argtypes = [I, L, P, P, P, P, P, P, L, L, L, P, L, L, P, P, P, L, P, P]
@@ -132,12 +137,18 @@ class Oracle:
         self.lib.oracle_qgemv_rows(fmt, gs, _p(w), _p(scales), _p(x), O, I, s, _p(rows), len(rows), _p(y))
         return y
 
-    def qgate_up(self, fmt: int, gs: int, wg, sg, wu, su, x, F: int, D: int) -> np.ndarray:
-        """h [s][F] = silu(gate x) * (up x) in double (step a4)."""
+    def glu(self, act: int, limit: float, g: float, u: float) -> float:
+        """The gate/up activation of one (g, u) pair: act 0 SwiGLU, act 1 clamped SwiGLU."""
+        return self.lib.oracle_glu(int(act), float(limit), float(g), float(u))
+
+    def qgate_up(self, fmt: int, gs: int, wg, sg, wu, su, x, F: int, D: int, act: int = 0,
+                 limit: float = 0.0) -> np.ndarray:
+        """h [s][F] = act(gate x, up x) in double (step a4; act 0 = silu(g) * u)."""
         wg, sg, wu, su, x = _u8(wg), _f32(sg), _u8(wu), _f32(su), _f32(x).reshape(-1, D)
         s = x.shape[0]
         h = np.empty((s, F), dtype=np.float64)
-        self.lib.oracle_qgate_up(fmt, gs, _p(wg), _p(sg), _p(wu), _p(su), _p(x), F, D, s, _p(h))
+        self.lib.oracle_qgate_up_act(fmt, gs, _p(wg), _p(sg), _p(wu), _p(su), _p(x), F, D, s, int(act),
+                                     float(limit), _p(h))
         return h
 
     def qgate_up_rows(self, fmt: int, gs: int, wg, sg, wu, su, x, F: int, D: int, rows) -> np.ndarray:
@@ -150,7 +161,8 @@ class Oracle:
         return h
 
     def expert_group(self, fmt: int, gs: int, gate, gate_s, up, up_s, down, down_s,
-                     E: int, D: int, F: int, x, ids, wts, cols=None) -> np.ndarray:
+                     E: int, D: int, F: int, x, ids, wts, cols=None, act: int = 0,
+                     limit: float = 0.0) -> np.ndarray:
         """out [s][D] (or [s][len(cols)]) in double (steps a4 + a5, rank order)."""
         gate, gate_s, up, up_s = _u8(gate), _f32(gate_s), _u8(up), _f32(up_s)
         down, down_s, x = _u8(down), _f32(down_s), _f32(x).reshape(-1, D)
@@ -165,9 +177,9 @@ class Oracle:
             ncols, cptr = len(cols), _p(cols)
         out = np.empty((s, ncols), dtype=np.float64)
         h = np.empty(F, dtype=np.float64)
-        self.lib.oracle_expert_group_cols(fmt, gs, _p(gate), _p(gate_s), _p(up), _p(up_s), _p(down),
-                                          _p(down_s), E, D, F, _p(x), s, k, _p(ids), _p(wts), cptr, ncols,
-                                          _p(out), _p(h))
+        self.lib.oracle_expert_group_act_cols(fmt, gs, _p(gate), _p(gate_s), _p(up), _p(up_s), _p(down),
+                                              _p(down_s), E, D, F, _p(x), s, k, _p(ids), _p(wts), int(act),
+                                              float(limit), cptr, ncols, _p(out), _p(h))
         return out
 
 
@@ -184,7 +196,7 @@ def default() -> Oracle:
 
 def __getattr__(name):
     # Module-level access to the default copy's methods: oracle.qgemv(...), ...
-    if name in {"threads", "packed_bytes", "codes", "e2m1", "code_value", "silu", "dequant_f32",
+    if name in {"threads", "packed_bytes", "codes", "e2m1", "code_value", "silu", "glu", "dequant_f32",
                 "qgemv", "qgemv_rows", "qgate_up", "qgate_up_rows", "expert_group"}:
         return getattr(default(), name)
     raise AttributeError(name)

@@ -243,6 +243,51 @@ def pin_gate_up(orc):
         _close(orc.qgate_up_rows(fmt, gs, pack(fmt, cg), sg, pack(fmt, cu), su, x, F, D, rows), got[:, rows])
 
 
+def pin_clamped_glu(orc):
+    """Clamped SwiGLU (reading: silu(min(g, L)) * clamp(u, -L, L)): its closed
+    cases and the structure a slip would break."""
+    grid = np.linspace(-9, 9, 37)
+    for g in grid:
+        for u in grid:
+            g, u = float(g), float(u)
+            # a limit at or above both values changes nothing (the plain case is pinned above)
+            assert orc.glu(1, 10.0, g, u) == orc.glu(0, 0.0, g, u)
+            # limit 0 zeroes everything (the page: clamps "at any limit, including 0")
+            assert orc.glu(1, 0.0, g, u) == 0.0
+            # past the limit the value no longer depends on g (from above) or u (both sides)
+            L = 2.0
+            if g > L:
+                assert orc.glu(1, L, g, u) == orc.glu(1, L, L, u)
+            if u > L:
+                assert orc.glu(1, L, g, u) == orc.glu(1, L, g, L)
+            if u < -L:
+                assert orc.glu(1, L, g, u) == orc.glu(1, L, g, -L)
+    # the gate is capped from above only: a very negative gate keeps its own silu
+    assert abs(orc.glu(1, 1.0, -5.0, 0.5) - (-5.0 * 0.0066928509242848554 * 0.5)) < 1e-15
+    # sigmoid(1) = 0.7310585786300049 (tables): g = 5 and u = 7 both clamp to L = 1
+    assert abs(orc.glu(1, 1.0, 5.0, 7.0) - 0.7310585786300049) < 1e-15
+    # the clamp of u is symmetric: u = -7 clamps to -1
+    assert abs(orc.glu(1, 1.0, 5.0, -7.0) + 0.7310585786300049) < 1e-15
+
+
+def pin_gate_up_clamped(orc):
+    rng = np.random.default_rng(37)
+    for fmt in ALL_FMTS:
+        F, D, s = 8, 128, 2
+        gs = group_of(fmt, D)
+        cg, cu = random_codes(fmt, F, D, rng), random_codes(fmt, F, D, rng)
+        sg = rng.lognormal(-3, 0.5, size=F * (D // gs)).astype(np.float32)
+        su = rng.lognormal(-3, 0.5, size=F * (D // gs)).astype(np.float32)
+        x = rng.standard_normal((s, D)).astype(np.float32)
+        g = x.astype(np.float64) @ dense(fmt, cg, sg, gs).T
+        u = x.astype(np.float64) @ dense(fmt, cu, su, gs).T
+        L = float(np.median(np.abs(u)))          # clamps about half of the values
+        got = orc.qgate_up(fmt, gs, pack(fmt, cg), sg, pack(fmt, cu), su, x, F, D, act=1, limit=L)
+        gc = np.minimum(g, L)
+        _close(got, gc * expit(gc) * np.clip(u, -L, L))
+        assert not orc.qgate_up(fmt, gs, pack(fmt, cg), sg, pack(fmt, cu), su, x, F, D, act=1, limit=0.0).any()
+
+
 # --- step a5: the routed expert group ----------------------------------------
 
 def _expert_store(fmt, E, D, F, rng):
@@ -300,8 +345,11 @@ def pin_expert_group(orc):
         # a sample of output columns equals those columns of the whole output
         cols = np.array([5, 127, 0])
         _close(orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, wts, cols=cols), got[:, cols], rtol=1e-14)
+        # clamped SwiGLU: a limit above every value is the plain group, limit 0 gives zeros
+        _close(orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, wts, act=1, limit=1e30), got, rtol=1e-15)
+        assert not orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, wts, act=1, limit=0.0).any()
 
 
 ALL_PINS = [pin_e2m1, pin_int4_nibbles, pin_int3_planes, pin_int8_bytes, pin_random_codes,
-            pin_dequant_f32, pin_fixed_groups, pin_gemv_bruteforce, pin_zero_scales, pin_linearity, pin_integer_exact,
-            pin_silu, pin_gate_up, pin_expert_group]
+            pin_dequant_f32, pin_fixed_groups, pin_gemv_bruteforce, pin_zero_scales, pin_linearity,
+            pin_integer_exact, pin_silu, pin_clamped_glu, pin_gate_up, pin_gate_up_clamped, pin_expert_group]

@@ -31,7 +31,10 @@ MUTANTS = {
     "gemv_token_ignored": ("y[t * O + o] = row_dot(fmt, gs, w, scales, O, I, o, x + t * I);",
                            "y[t * O + o] = row_dot(fmt, gs, w, scales, O, I, o, x);"),
     "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
-    "gate_up_swapped": ("h[t * F + f] = oracle_silu(g) * u;", "h[t * F + f] = oracle_silu(u) * g;"),
+    "gate_up_swapped": ("return oracle_silu(g) * u;", "return oracle_silu(u) * g;"),
+    "clamp_up_one_sided": ("if (u < -limit) u = -limit;", "if (u < 0.0) u = 0.0;"),
+    "clamp_gate_missing": ("if (g > limit) g = limit;", ""),
+    "clamp_gate_both_sides": ("if (g > limit) g = limit;", "if (g > limit) g = limit;\n        if (g < -limit) g = -limit;"),
     "router_weight_dropped": ("out[t * ncols + j] += wr * z;", "out[t * ncols + j] += z;"),
     "down_transposed": ("oracle_weight(fmt, gs, de, dse, D, F, d, f)", "oracle_weight(fmt, gs, de, dse, F, D, f, d)"),
     "expert_rank_last_only": ("out[t * ncols + j] = 0.0;", "out[t * ncols + j] = 0.0 * out[t * ncols + j];"),
