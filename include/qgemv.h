@@ -83,8 +83,20 @@ enum {
     QSTATUS_WORKSPACE = -5,      /* workspace smaller than qexpert_group_workspace() */
     QSTATUS_LAUNCH = -6,         /* CUDA reported an error at launch */
     QSTATUS_DEVICE_TIMEOUT = -7, /* a bounded device-side wait ran out */
-    QSTATUS_BAD_EXPERT_ID = -8   /* an expert id outside [0, E) (reported on the device) */
+    QSTATUS_BAD_EXPERT_ID = -8,  /* an expert id outside [0, E) (reported on the device) */
+    QSTATUS_BAD_ACT = -9         /* unknown activation, or a limit that is negative or NaN */
 };
+
+/*
+ * Activations of the gate/up product (h = act(g, u), g = gate x, u = up x):
+ *   QACT_SWIGLU          silu(g) * u, silu(z) = z / (1 + e^-z)
+ *   QACT_SWIGLU_CLAMPED  silu(min(g, L)) * min(max(u, -L), L) for a limit
+ *                        L >= 0 -- the swiglu_limit of the models in colibri
+ *                        docs/vulkan.md (expert-tier paragraph on GLM-5.3
+ *                        Flash); L = 0 gives zeros, L = +inf is SwiGLU.
+ */
+#define QACT_SWIGLU 0
+#define QACT_SWIGLU_CLAMPED 1
 
 /*
  * y[t][o] = sum_i value(W[o][i]) * scales[o][i/gs] * x[t][i],  t < s, o < O.
@@ -106,6 +118,13 @@ int qgemv(int fmt, int gs, const void* w, const float* scales,
 int qgate_up(int fmt, int gs, const void* wg, const float* sg,
              const void* wu, const float* su,
              const float* x, int F, int D, int s, float* h, void* stream);
+
+/* qgate_up with the activation act (QACT_*) and its limit (read only for
+ * QACT_SWIGLU_CLAMPED).  QSTATUS_BAD_ACT for an unknown act or a negative or
+ * NaN limit of the clamped one. */
+int qgate_up_act(int fmt, int gs, const void* wg, const float* sg,
+                 const void* wu, const float* su,
+                 const float* x, int F, int D, int s, int act, float limit, float* h, void* stream);
 
 /* Bytes of workspace qexpert_group needs for these sizes. */
 size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
@@ -136,6 +155,18 @@ int qexpert_group(int fmt, int gs,
                   const int32_t* ids, const float* wts,
                   float* out, void* workspace, size_t ws_bytes,
                   int32_t* status_dev, void* stream);
+
+/* qexpert_group with the activation act (QACT_*) and its limit in place of
+ * silu(g) * u; QSTATUS_BAD_ACT as for qgate_up_act. */
+int qexpert_group_act(int fmt, int gs,
+                      const void* gate, const float* gate_s,
+                      const void* up, const float* up_s,
+                      const void* down, const float* down_s,
+                      int E, int D, int F,
+                      const float* x, int s, int k,
+                      const int32_t* ids, const float* wts, int act, float limit,
+                      float* out, void* workspace, size_t ws_bytes,
+                      int32_t* status_dev, void* stream);
 
 /*
  * qexpert_group for callers that cannot allocate device memory -- for

@@ -38,8 +38,8 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for st in range(0, -9, -1):
-        assert _lib.qstatus_string(st)
+    for st in range(0, -10, -1):
+        assert _lib.qstatus_string(st) and "unknown status" not in _lib.qstatus_string(st)
     assert "unknown" in _lib.qstatus_string(-100)
 
 
@@ -99,6 +99,22 @@ def test_expert_group_checks(L):
     bad[10] = 2050                                     # F not a multiple of the group
     assert L.qexpert_group(*bad) == -2
     assert _lib.qexpert_group_workspace(0, 6144, 2048, 8, 8) >= 0
+
+
+def test_activation_checks(L):
+    """Unknown activations and limits that are negative or NaN are refused before any launch."""
+    gu = lambda act, lim: L.qgate_up_act(4, 32, A, A, A, A, A, 16, 1024, 1, act, lim, A, None)
+    assert gu(2, 1.0) == -9
+    assert gu(1, -0.5) == -9
+    assert gu(1, float("nan")) == -9
+    assert gu(1, -0.5) == L.qgate_up_act(4, 32, A, A, A, A, A, 16, 1024, 1, 1, -0.5, A, None)
+    # a bad activation is reported before a bad size
+    assert L.qgate_up_act(4, 32, A, A, A, A, A, 16, 1000, 1, 3, 1.0, A, None) == -9
+    ws = _lib.qexpert_group_workspace(256, 6144, 2048, 8, 8)
+    args = [4, 32, A, A, A, A, A, A, 256, 6144, 2048, A, 8, 8, A, A, 1, float("nan"), A, A, ws, None, None]
+    assert L.qexpert_group_act(*args) == -9
+    args[16], args[17] = 7, 1.0
+    assert L.qexpert_group_act(*args) == -9
 
 
 def test_kernel_policy_round_trip(L):

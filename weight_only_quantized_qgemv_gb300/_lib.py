@@ -25,7 +25,10 @@ QSTATUS = {
     -6: "QSTATUS_LAUNCH",
     -7: "QSTATUS_DEVICE_TIMEOUT",
     -8: "QSTATUS_BAD_EXPERT_ID",
+    -9: "QSTATUS_BAD_ACT",
 }
+
+QACT_SWIGLU, QACT_SWIGLU_CLAMPED = 0, 1
 
 
 class QStatusError(RuntimeError):
@@ -59,6 +62,11 @@ def lib() -> ctypes.CDLL:
         L.qexpert_group_workspace.restype = Z
         L.qexpert_group.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, P, P, P, P, Z, P, P]
         L.qexpert_group.restype = I
+        Fl = ctypes.c_float
+        L.qgate_up_act.argtypes = [I, I, P, P, P, P, P, I, I, I, I, Fl, P, P]
+        L.qgate_up_act.restype = I
+        L.qexpert_group_act.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, P, P, I, Fl, P, P, Z, P, P]
+        L.qexpert_group_act.restype = I
         L.qdequant.argtypes = [I, I, P, P, I, I, P, P]
         L.qdequant.restype = I
         L.qstatus_string.argtypes = [I]
@@ -129,6 +137,11 @@ def qgate_up(fmt, gs, wg, sg, wu, su, x, F, D, s, h, stream=None):
                           _stream(stream)))
 
 
+def qgate_up_act(fmt, gs, wg, sg, wu, su, x, F, D, s, act, limit, h, stream=None):
+    _check(lib().qgate_up_act(fmt, gs, _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(x), F, D, s, int(act),
+                              float(limit), _ptr(h), _stream(stream)))
+
+
 def qexpert_group_workspace(E, D, F, s, k) -> int:
     return lib().qexpert_group_workspace(E, D, F, s, k)
 
@@ -138,6 +151,14 @@ def qexpert_group(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, 
     _check(lib().qexpert_group(fmt, gs, _ptr(gate), _ptr(gate_s), _ptr(up), _ptr(up_s), _ptr(down),
                                _ptr(down_s), E, D, F, _ptr(x), s, k, _ptr(ids), _ptr(wts), _ptr(out),
                                _ptr(workspace), ws_bytes, _ptr(status_dev), _stream(stream)))
+
+
+def qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, act, limit,
+                      out, workspace, ws_bytes, status_dev=None, stream=None):
+    _check(lib().qexpert_group_act(fmt, gs, _ptr(gate), _ptr(gate_s), _ptr(up), _ptr(up_s), _ptr(down),
+                                   _ptr(down_s), E, D, F, _ptr(x), s, k, _ptr(ids), _ptr(wts), int(act),
+                                   float(limit), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status_dev),
+                                   _stream(stream)))
 
 
 def qdequant(fmt, gs, w, scales, O, I, out, stream=None):

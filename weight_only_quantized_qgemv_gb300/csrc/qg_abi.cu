@@ -72,6 +72,15 @@ constexpr int kMaxI = 51200;   // an upper bound; the shared-memory budget below
 
 // Shared memory left for activation rows once the copy rings of a launch of
 // format fmt with nm matrices per row tile are placed.
+// QSTATUS_BAD_ACT unless act is a QACT_* and, for the clamped one, the limit
+// is a number >= 0 (+inf allowed).
+static int check_act(int act, float limit)
+{
+    if (act == QACT_SWIGLU) return QSTATUS_OK;
+    if (act == QACT_SWIGLU_CLAMPED) return (limit >= 0.0f) ? QSTATUS_OK : QSTATUS_BAD_ACT;   // NaN fails too
+    return QSTATUS_BAD_ACT;
+}
+
 static size_t ring_bytes(int fmt, int nm)
 {
     switch (fmt) {
@@ -282,6 +291,7 @@ const char* qstatus_string(int status)
     case QSTATUS_LAUNCH: return "CUDA reported an error at launch (see qlast_cuda_error)";
     case QSTATUS_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case QSTATUS_BAD_EXPERT_ID: return "an expert id is outside [0, E)";
+    case QSTATUS_BAD_ACT: return "unknown activation, or a clamp limit that is negative or NaN";
     default: return "unknown status";
     }
 }
@@ -335,8 +345,16 @@ int qgemv(int fmt, int gs, const void* w, const float* scales, const float* x, i
 int qgate_up(int fmt, int gs, const void* wg, const float* sg, const void* wu, const float* su, const float* x,
              int F, int D, int s, float* h, void* stream)
 {
+    return qgate_up_act(fmt, gs, wg, sg, wu, su, x, F, D, s, QACT_SWIGLU, 0.0f, h, stream);
+}
+
+int qgate_up_act(int fmt, int gs, const void* wg, const float* sg, const void* wu, const float* su,
+                 const float* x, int F, int D, int s, int act, float limit, float* h, void* stream)
+{
+    int st = check_act(act, limit);
+    if (st) return st;
     int g = 0;
-    int st = check_fmt(fmt, gs, D, &g);
+    st = check_fmt(fmt, gs, D, &g);
     if (st) return st;
     if (F < 1 || D < 1 || s < 1 || D > kMaxI) return QSTATUS_BAD_DIM;
     if (!wg || !sg || !wu || !su || !x || !h) return QSTATUS_NULL;
@@ -353,7 +371,7 @@ int qgate_up(int fmt, int gs, const void* wg, const float* sg, const void* wu, c
     for (int s0 = 0; s0 < s; s0 += per) {
         const int n = s - s0 < per ? s - s0 : per;
         cudaError_t e;
-#define QG_CALL(name) gate_up_##name(mg, mu, x + (size_t)s0 * D, n, h + (size_t)s0 * F, F, grid, cs)
+#define QG_CALL(name) gate_up_##name(mg, mu, x + (size_t)s0 * D, n, h + (size_t)s0 * F, F, act, limit, grid, cs)
         QG_FMT_SWITCH(fmt, QG_CALL)
 #undef QG_CALL
         if (e != cudaSuccess) return launch_status(e);
@@ -373,8 +391,19 @@ int qexpert_group(int fmt, int gs, const void* gate, const float* gate_s, const 
                   const int32_t* ids, const float* wts, float* out, void* workspace, size_t ws_bytes,
                   int32_t* status_dev, void* stream)
 {
+    return qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts,
+                             QACT_SWIGLU, 0.0f, out, workspace, ws_bytes, status_dev, stream);
+}
+
+int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, const void* up, const float* up_s,
+                      const void* down, const float* down_s, int E, int D, int F, const float* x, int s, int k,
+                      const int32_t* ids, const float* wts, int act, float limit, float* out, void* workspace,
+                      size_t ws_bytes, int32_t* status_dev, void* stream)
+{
+    int st = check_act(act, limit);
+    if (st) return st;
     int g_up = 0, g_dn = 0;
-    int st = check_fmt(fmt, gs, D, &g_up);
+    st = check_fmt(fmt, gs, D, &g_up);
     if (st) return st;
     st = check_fmt(fmt, gs, F, &g_dn);
     if (st) return st;
@@ -394,6 +423,8 @@ int qexpert_group(int fmt, int gs, const void* gate, const float* gate_s, const 
 
     ExpertArgs a;
     a.grid = grid;
+    a.act = act;
+    a.limit = limit;
     int r_up = 1, r_dn = 1;
     switch (fmt) {
     case QFMT_INT8_ROW: r_up = tile_rows_int8(2); r_dn = tile_rows_int8(1); break;

@@ -118,6 +118,8 @@ struct DenseJob : RingLayout, TileSource<NM> {
     float* y;            // y[s * ldy + row]
     long long ldy;
     int S;
+    int act;             // NM = 2: QACT_* of the gate/up product
+    float limit;
 
     __device__ bool bad() const { return false; }
     __device__ int nbatch() const { return 1; }
@@ -159,6 +161,8 @@ struct ExpertUpJob : RingLayout, TileSource<2> {
     const int32_t* bounds;          // CTA tile bounds of this phase (G + 1 entries)
     float* h;
     int D, F;
+    int act;                        // QACT_* of the gate/up product
+    float limit;
 
     __device__ bool bad() const { return hdr[0] != 0; }
     __device__ int nbatch() const { return hdr[1]; }
@@ -250,11 +254,16 @@ struct Sink {
     __device__ __forceinline__ void put(float v, int idx, bool lane_ok, long long tile_row0, long long row_end) const
     {
         if constexpr (NM == 2) {
-            const float u = __shfl_xor_sync(0xffffffffu, v, V / 2);
+            float u = __shfl_xor_sync(0xffffffffu, v, V / 2);
             if (lane_ok && !(idx & 1) && idx < S * R * 2) {
                 const int sr = idx >> 1, s = sr / R, r = sr - (sr / R) * R;
                 const long long row = tile_row0 + r;
-                if (row < row_end && s < s_act) job.store(b, s, row, v / (1.0f + expf(-v)) * u);
+                float g = v;
+                if (job.act == QACT_SWIGLU_CLAMPED) {    // clamped SwiGLU: gate capped, up clamped to [-L, L]
+                    g = fminf(g, job.limit);
+                    u = fminf(fmaxf(u, -job.limit), job.limit);
+                }
+                if (row < row_end && s < s_act) job.store(b, s, row, g / (1.0f + expf(-g)) * u);
             }
         } else {
             if (lane_ok && idx < S * R) {
@@ -568,6 +577,8 @@ cudaError_t QG_CAT(gemv_, QG_NAME)(const HostMat& hm, const float* x, int s, flo
                                    cudaStream_t st)
 {
     DenseJob<1> job;
+    job.act = QACT_SWIGLU;
+    job.limit = 0.0f;
     job.m[0] = to_mat(hm);
     job.x = x;
     job.y = y;
@@ -579,9 +590,11 @@ cudaError_t QG_CAT(gemv_, QG_NAME)(const HostMat& hm, const float* x, int s, flo
 }
 
 cudaError_t QG_CAT(gate_up_, QG_NAME)(const HostMat& g, const HostMat& u, const float* x, int s, float* h,
-                                      long long ldh, int grid, cudaStream_t st)
+                                      long long ldh, int act, float limit, int grid, cudaStream_t st)
 {
     DenseJob<2> job;
+    job.act = act;
+    job.limit = limit;
     job.m[0] = to_mat(g);
     job.m[1] = to_mat(u);
     job.x = x;
@@ -610,6 +623,8 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
     job.pair_tok = reinterpret_cast<const int32_t*>(a.ws + L.pair_tok);
     job.h = reinterpret_cast<float*>(a.ws + L.h);
     job.bounds = reinterpret_cast<const int32_t*>(a.ws + L.bounds);
+    job.act = a.act;
+    job.limit = a.limit;
     job.D = a.D;
     job.F = a.F;
     job.ring_off = (int)align16((size_t)a.smax * a.D * sizeof(float));

@@ -69,6 +69,8 @@ inline WsLayout ws_layout(int D, int F, int s, int k)
 
 struct ExpertArgs {
     int gs;
+    int act;           // QACT_* of the gate/up product
+    float limit;       // its limit (QACT_SWIGLU_CLAMPED)
     const void *gate, *up, *down;
     const float *gate_s, *up_s, *down_s;
     int E, D, F, s, k;
@@ -115,7 +117,7 @@ bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long lo
     cudaError_t gemv_##name(const HostMat& m, const float* x, int s, float* y, long long ldy,          \
                             int grid, cudaStream_t st);                                                \
     cudaError_t gate_up_##name(const HostMat& g, const HostMat& u, const float* x, int s, float* h,    \
-                               long long ldh, int grid, cudaStream_t st);                              \
+                               long long ldh, int act, float limit, int grid, cudaStream_t st);        \
     cudaError_t expert_up_##name(const ExpertArgs& a, int grid, cudaStream_t st);                       \
     cudaError_t expert_down_##name(const ExpertArgs& a, int grid, cudaStream_t st);                     \
     cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);                         \
