@@ -225,10 +225,13 @@ class GemvBench:
 
 
 class ExpertBench:
-    def __init__(self, wl, device, nsteps):
+    def __init__(self, wl, device, nsteps, swiglu_limit=None):
         import torch
-        from weight_only_quantized_qgemv_gb300 import qexpert_group_workspace
+        from weight_only_quantized_qgemv_gb300 import QACT_SWIGLU, QACT_SWIGLU_CLAMPED, qexpert_group_workspace
         self.wl = wl
+        # activation: SwiGLU, or clamped SwiGLU with the given limit
+        self.act = QACT_SWIGLU if swiglu_limit is None else QACT_SWIGLU_CLAMPED
+        self.limit = 0.0 if swiglu_limit is None else float(swiglu_limit)
         self.torch = torch
         self.d = {}
         for name, which in wl.MATRICES:
@@ -265,11 +268,11 @@ class ExpertBench:
         self.launches_per_step = 4
 
     def _call(self, r, x, ids, wts, stream):
-        from weight_only_quantized_qgemv_gb300 import qexpert_group
+        from weight_only_quantized_qgemv_gb300 import qexpert_group_act
         wl, d = self.wl, self.d
-        qexpert_group(wl.fmt, self.gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"],
-                      wl.E, wl.D, wl.F, x, wl.s, wl.k, ids, wts, self.out, self.ws, self.ws_bytes,
-                      self.status, stream)
+        qexpert_group_act(wl.fmt, self.gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"],
+                          wl.E, wl.D, wl.F, x, wl.s, wl.k, ids, wts, self.act, self.limit, self.out, self.ws,
+                          self.ws_bytes, self.status, stream)
 
     def step(self, i, stream):
         r = i % self.nroutes
@@ -303,13 +306,14 @@ class ExpertBench:
         cfg = expert_config(wl)
         cfg["l2"] = f"{self.nroutes} seeded routings over the {wl.E * self.expert_bytes / 1e9:.2f} GB store (> L2)"
         cfg["mean_experts_per_step"] = float(np.mean([len(np.unique(r)) for r in self.ids_host]))
+        cfg["activation"] = "swiglu" if self.act == 0 else f"swiglu clamped at {self.limit:g}"
         return cfg
 
 
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample
 # ---------------------------------------------------------------------------
-def oracle_sample_runner(wl, target_s: float):
+def oracle_sample_runner(wl, target_s: float, swiglu_limit=None):
     """A callable running the oracle on a sample of the workload, the bytes it
     covers, and a description.  Sized to ~target_s seconds."""
     from oracle import oracle as orc
@@ -340,7 +344,8 @@ def oracle_sample_runner(wl, target_s: float):
 
     def run_rows(nrows, start=0):
         rows = (np.arange(nrows) + start) % wl.F
-        orc.qgate_up_rows(wl.fmt, wl.gs, st["gate"], st["gate_s"], st["up"], st["up_s"], x, wl.F, wl.D, rows)
+        orc.qgate_up_rows(wl.fmt, wl.gs, st["gate"], st["gate_s"], st["up"], st["up_s"], x, wl.F, wl.D, rows,
+                          act=0 if swiglu_limit is None else 1, limit=swiglu_limit or 0.0)
         return nrows * per_row
 
     t = time.perf_counter()
@@ -351,11 +356,11 @@ def oracle_sample_runner(wl, target_s: float):
             f"{nrows} gate/up rows (cycling over the {wl.F} rows) of expert {int(ids[0, 0])} (token 0, first routing)")
 
 
-def cpu_baseline(wl, target_s=12.0):
+def cpu_baseline(wl, target_s=12.0, swiglu_limit=None):
     """The oracle on the host cores: samples of about a second, repeated until
     about target_s seconds of CPU work."""
     from oracle import oracle as orc
-    run, desc = oracle_sample_runner(wl, min(1.0, target_s))
+    run, desc = oracle_sample_runner(wl, min(1.0, target_s), swiglu_limit)
     t = time.perf_counter()
     nbytes, n = 0, 0
     while True:
@@ -374,7 +379,7 @@ def reference_arm(args, wl, world, rank):
     from oracle import oracle as orc
     orc.build()
     target = args.sample_seconds if args.sample_seconds else max(0.5, 60.0 / max(1, args.steps + args.warmup))
-    run, desc = oracle_sample_runner(wl, target_s=target)
+    run, desc = oracle_sample_runner(wl, target_s=target, swiglu_limit=args.swiglu_limit)
     for i in range(args.warmup):
         run(i)
     t = time.perf_counter()
@@ -423,6 +428,8 @@ def main():
     ap.add_argument("--graph-len", type=int, default=64, help="calls captured per CUDA graph replay")
     ap.add_argument("--sample-seconds", type=float, default=None,
                     help="CPU seconds per oracle sample (reference arm / CPU baseline)")
+    ap.add_argument("--swiglu-limit", type=float, default=None,
+                    help="expert workloads: clamped SwiGLU with this limit instead of SwiGLU")
     args = ap.parse_args()
     wl = synth.workload(args.workload)
     world, rank, local = dist_env()
@@ -455,7 +462,8 @@ def main():
 
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024
-    bench = GemvBench(wl, device, l2) if isinstance(wl, synth.GemvWorkload) else ExpertBench(wl, device, args.steps)
+    bench = (GemvBench(wl, device, l2) if isinstance(wl, synth.GemvWorkload)
+             else ExpertBench(wl, device, args.steps, args.swiglu_limit))
     stream = torch.cuda.Stream(device)
 
     # warm-up: eager steps, then build the graph (its capture also warms up)
@@ -524,7 +532,7 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.sample_seconds or 12.0)
+        cpu = cpu_baseline(wl, args.sample_seconds or 12.0, args.swiglu_limit)
     cfg = bench.config()
     cfg["graph_calls_per_replay"] = G
     line = {

@@ -224,17 +224,25 @@ void oracle_qgate_up(int fmt, long gs, const uint8_t *wg, const float *sg,
 }
 
 /* Step a4 on a sample of rows f = rows[j]. */
-void oracle_qgate_up_rows(int fmt, long gs, const uint8_t *wg, const float *sg,
-                          const uint8_t *wu, const float *su, const float *x,
-                          long F, long D, long s, const long *rows, long nrows, double *h)
+void oracle_qgate_up_rows_act(int fmt, long gs, const uint8_t *wg, const float *sg,
+                              const uint8_t *wu, const float *su, const float *x,
+                              long F, long D, long s, const long *rows, long nrows, int act, double limit,
+                              double *h)
 {
 #pragma omp parallel for schedule(static)
     for (long j = 0; j < nrows; j++)
         for (long t = 0; t < s; t++) {
             double g = row_dot(fmt, gs, wg, sg, F, D, rows[j], x + t * D);
             double u = row_dot(fmt, gs, wu, su, F, D, rows[j], x + t * D);
-            h[t * nrows + j] = oracle_silu(g) * u;
+            h[t * nrows + j] = oracle_glu(act, limit, g, u);
         }
+}
+
+void oracle_qgate_up_rows(int fmt, long gs, const uint8_t *wg, const float *sg,
+                          const uint8_t *wu, const float *su, const float *x,
+                          long F, long D, long s, const long *rows, long nrows, double *h)
+{
+    oracle_qgate_up_rows_act(fmt, gs, wg, sg, wu, su, x, F, D, s, rows, nrows, 0, 0.0, h);
 }
 
 /* Steps a4 + a5 ([GUIDE] API contract, coli_vk_expert_group; [VULKAN] the sum

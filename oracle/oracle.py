@@ -81,6 +81,7 @@ class Oracle:
         lib.oracle_glu.argtypes = [I, D, D, D]
         lib.oracle_glu.restype = D
         lib.oracle_qgate_up_act.argtypes = [I, L, P, P, P, P, P, L, L, L, I, D, P]
+        lib.oracle_qgate_up_rows_act.argtypes = [I, L, P, P, P, P, P, L, L, L, P, L, I, D, P]
         lib.oracle_expert_group_act_cols.argtypes = [I, L, P, P, P, P, P, P, L, L, L, P, L, L, P, P, I, D, P, L,
                                                      P, P]
         lib.oracle_qgate_up.argtypes = [I, L, P, P, P, P, P, L, L, L, P]
@@ -151,13 +152,14 @@ class Oracle:
                                      float(limit), _p(h))
         return h
 
-    def qgate_up_rows(self, fmt: int, gs: int, wg, sg, wu, su, x, F: int, D: int, rows) -> np.ndarray:
+    def qgate_up_rows(self, fmt: int, gs: int, wg, sg, wu, su, x, F: int, D: int, rows, act: int = 0,
+                      limit: float = 0.0) -> np.ndarray:
         wg, sg, wu, su, x = _u8(wg), _f32(sg), _u8(wu), _f32(su), _f32(x).reshape(-1, D)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         s = x.shape[0]
         h = np.empty((s, len(rows)), dtype=np.float64)
-        self.lib.oracle_qgate_up_rows(fmt, gs, _p(wg), _p(sg), _p(wu), _p(su), _p(x), F, D, s,
-                                      _p(rows), len(rows), _p(h))
+        self.lib.oracle_qgate_up_rows_act(fmt, gs, _p(wg), _p(sg), _p(wu), _p(su), _p(x), F, D, s,
+                                          _p(rows), len(rows), int(act), float(limit), _p(h))
         return h
 
     def expert_group(self, fmt: int, gs: int, gate, gate_s, up, up_s, down, down_s,
