@@ -47,17 +47,23 @@
 #include <stdint.h>
 
 #define ORACLE_INT8_ROW 1
+#define ORACLE_INT4_ROW 2
 #define ORACLE_INT4_G 4
 #define ORACLE_INT3_G64 5
 #define ORACLE_MXFP4_G32 7
+#define ORACLE_MXFP4_E8M0 8
+#define ORACLE_INT8_G 13
 
 /* Bytes of one packed O x I matrix in format fmt ([GUIDE] shader details). */
 long oracle_packed_bytes(int fmt, long O, long I)
 {
     switch (fmt) {
-    case ORACLE_INT8_ROW: return O * I;            /* one byte per code */
+    case ORACLE_INT8_ROW:
+    case ORACLE_INT8_G: return O * I;              /* one byte per code */
+    case ORACLE_INT4_ROW:
     case ORACLE_INT4_G:
-    case ORACLE_MXFP4_G32: return O * I / 2;       /* two codes per byte */
+    case ORACLE_MXFP4_G32:
+    case ORACLE_MXFP4_E8M0: return O * I / 2;      /* two codes per byte */
     case ORACLE_INT3_G64: return O * I / 4 + O * I / 8; /* plane A + plane B */
     default: return -1;
     }
@@ -68,10 +74,13 @@ int oracle_code(int fmt, const uint8_t *w, long O, long I, long o, long i)
 {
     switch (fmt) {
     case ORACLE_INT8_ROW:
+    case ORACLE_INT8_G:
         /* one signed byte per code */
         return (int)(int8_t)w[o * I + i];
+    case ORACLE_INT4_ROW:
     case ORACLE_INT4_G:
-    case ORACLE_MXFP4_G32: {
+    case ORACLE_MXFP4_G32:
+    case ORACLE_MXFP4_E8M0: {
         /* two codes per byte: even i in the low nibble, odd i in the high one */
         uint8_t b = w[o * (I / 2) + i / 2];
         return (i % 2 == 0) ? (b & 0x0F) : ((b >> 4) & 0x0F);
@@ -103,31 +112,46 @@ double oracle_e2m1(int c)
 double oracle_code_value(int fmt, int code)
 {
     switch (fmt) {
-    case ORACLE_INT8_ROW: return (double)code;          /* int8 as is */
+    case ORACLE_INT8_ROW:
+    case ORACLE_INT8_G: return (double)code;            /* int8 as is */
+    case ORACLE_INT4_ROW:
     case ORACLE_INT4_G: return (double)(code - 8);      /* offset binary, nibble - 8 */
     case ORACLE_INT3_G64: return (double)(code - 4);    /* 3-bit code - 4 */
-    case ORACLE_MXFP4_G32: return oracle_e2m1(code);    /* e2m1 element */
+    case ORACLE_MXFP4_G32:
+    case ORACLE_MXFP4_E8M0: return oracle_e2m1(code);   /* e2m1 element */
     default: return 0.0;
     }
 }
 
-/* Group size of a format: int8 per row has one group per row; int3-g64
- * groups 64 inputs and MXFP4 32 ([GUIDE] shader details); int4 takes gs. */
+/* Group size of a format: int8 and int4 per row have one group per row;
+ * int3-g64 groups 64 inputs and MXFP4 32 ([GUIDE] shader details); grouped
+ * int4 and int8 take gs. */
 static long group_of(int fmt, long I, long gs)
 {
     switch (fmt) {
-    case ORACLE_INT8_ROW: return I;
+    case ORACLE_INT8_ROW:
+    case ORACLE_INT4_ROW: return I;
     case ORACLE_INT3_G64: return 64;
-    case ORACLE_MXFP4_G32: return 32;
+    case ORACLE_MXFP4_G32:
+    case ORACLE_MXFP4_E8M0: return 32;
     default: return gs;
     }
 }
 
-/* The scale of element (o, i): one f32 per group of gs inputs along the row,
- * stored row-major [O][I/gs]. */
+/* ue8m0 scale byte (OCP microscaling): 2^(e - 127); e = 255 is NaN. */
+double oracle_e8m0(int e)
+{
+    return e == 255 ? NAN : ldexp(1.0, e - 127);
+}
+
+/* The scale of element (o, i): one per group of gs inputs along the row,
+ * stored row-major [O][I/gs]: f32, or for MXFP4_E8M0 one ue8m0 byte
+ * ([VULKAN] model table: the checkpoints' MXFP4 with ue8m0 scales). */
 static double scale_of(int fmt, const float *scales, long I, long gs, long o, long i)
 {
     gs = group_of(fmt, I, gs);
+    if (fmt == ORACLE_MXFP4_E8M0)
+        return oracle_e8m0(((const uint8_t *)scales)[o * (I / gs) + i / gs]);
     return (double)scales[o * (I / gs) + i / gs];
 }
 
@@ -275,9 +299,11 @@ void oracle_expert_group_act_cols(int fmt, long gs,
             const uint8_t *ge = gate + e * gu_bytes;
             const uint8_t *ue = up + e * gu_bytes;
             const uint8_t *de = down + e * dn_bytes;
-            const float *gse = gate_s + e * gu_scales;
-            const float *use = up_s + e * gu_scales;
-            const float *dse = down_s + e * dn_scales;
+            /* expert e's scales: e * (scales per matrix) elements of f32, or of one byte for ue8m0 */
+            long ssz = fmt == ORACLE_MXFP4_E8M0 ? 1 : (long)sizeof(float);
+            const float *gse = (const float *)((const uint8_t *)gate_s + e * gu_scales * ssz);
+            const float *use = (const float *)((const uint8_t *)up_s + e * gu_scales * ssz);
+            const float *dse = (const float *)((const uint8_t *)down_s + e * dn_scales * ssz);
             double wr = (double)wts[t * k + r];
 #pragma omp parallel for schedule(static)
             for (long f = 0; f < F; f++) {

@@ -52,6 +52,11 @@ def _u8(a):
     return np.ascontiguousarray(a, dtype=np.uint8)
 
 
+def _sc(fmt, a):
+    """Scales as the format stores them: ue8m0 bytes for MXFP4_E8M0 (8), else f32."""
+    return _u8(a) if fmt == 8 else _f32(a)
+
+
 def _f32(a):
     return np.ascontiguousarray(a, dtype=np.float32)
 
@@ -76,6 +81,8 @@ class Oracle:
         lib.oracle_dequant_f32.argtypes = [I, L, P, P, L, L, P]
         lib.oracle_qgemv.argtypes = [I, L, P, P, P, L, L, L, P]
         lib.oracle_qgemv_rows.argtypes = [I, L, P, P, P, L, L, L, P, L, P]
+        lib.oracle_e8m0.argtypes = [I]
+        lib.oracle_e8m0.restype = D
         lib.oracle_silu.argtypes = [D]
         lib.oracle_silu.restype = D
         lib.oracle_glu.argtypes = [I, D, D, D]
@@ -116,14 +123,14 @@ class Oracle:
 
     def dequant_f32(self, fmt: int, gs: int, w, scales, O: int, I: int) -> np.ndarray:
         """Dequantized weights rounded once to f32 [O][I] (step a2)."""
-        w, scales = _u8(w), _f32(scales)
+        w, scales = _u8(w), _sc(fmt, scales)
         out = np.empty((O, I), dtype=np.float32)
         self.lib.oracle_dequant_f32(fmt, gs, _p(w), _p(scales), O, I, _p(out))
         return out
 
     def qgemv(self, fmt: int, gs: int, w, scales, x, O: int, I: int) -> np.ndarray:
         """y [s][O] in double (step a3)."""
-        w, scales, x = _u8(w), _f32(scales), _f32(x).reshape(-1, I)
+        w, scales, x = _u8(w), _sc(fmt, scales), _f32(x).reshape(-1, I)
         s = x.shape[0]
         y = np.empty((s, O), dtype=np.float64)
         self.lib.oracle_qgemv(fmt, gs, _p(w), _p(scales), _p(x), O, I, s, _p(y))
@@ -131,12 +138,16 @@ class Oracle:
 
     def qgemv_rows(self, fmt: int, gs: int, w, scales, x, O: int, I: int, rows) -> np.ndarray:
         """y [s][len(rows)] for the sampled rows."""
-        w, scales, x = _u8(w), _f32(scales), _f32(x).reshape(-1, I)
+        w, scales, x = _u8(w), _sc(fmt, scales), _f32(x).reshape(-1, I)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         s = x.shape[0]
         y = np.empty((s, len(rows)), dtype=np.float64)
         self.lib.oracle_qgemv_rows(fmt, gs, _p(w), _p(scales), _p(x), O, I, s, _p(rows), len(rows), _p(y))
         return y
+
+    def e8m0(self, e: int) -> float:
+        """Value of a ue8m0 scale byte."""
+        return self.lib.oracle_e8m0(int(e))
 
     def glu(self, act: int, limit: float, g: float, u: float) -> float:
         """The gate/up activation of one (g, u) pair: act 0 SwiGLU, act 1 clamped SwiGLU."""
@@ -145,7 +156,7 @@ class Oracle:
     def qgate_up(self, fmt: int, gs: int, wg, sg, wu, su, x, F: int, D: int, act: int = 0,
                  limit: float = 0.0) -> np.ndarray:
         """h [s][F] = act(gate x, up x) in double (step a4; act 0 = silu(g) * u)."""
-        wg, sg, wu, su, x = _u8(wg), _f32(sg), _u8(wu), _f32(su), _f32(x).reshape(-1, D)
+        wg, sg, wu, su, x = _u8(wg), _sc(fmt, sg), _u8(wu), _sc(fmt, su), _f32(x).reshape(-1, D)
         s = x.shape[0]
         h = np.empty((s, F), dtype=np.float64)
         self.lib.oracle_qgate_up_act(fmt, gs, _p(wg), _p(sg), _p(wu), _p(su), _p(x), F, D, s, int(act),
@@ -154,7 +165,7 @@ class Oracle:
 
     def qgate_up_rows(self, fmt: int, gs: int, wg, sg, wu, su, x, F: int, D: int, rows, act: int = 0,
                       limit: float = 0.0) -> np.ndarray:
-        wg, sg, wu, su, x = _u8(wg), _f32(sg), _u8(wu), _f32(su), _f32(x).reshape(-1, D)
+        wg, sg, wu, su, x = _u8(wg), _sc(fmt, sg), _u8(wu), _sc(fmt, su), _f32(x).reshape(-1, D)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         s = x.shape[0]
         h = np.empty((s, len(rows)), dtype=np.float64)
@@ -166,8 +177,8 @@ class Oracle:
                      E: int, D: int, F: int, x, ids, wts, cols=None, act: int = 0,
                      limit: float = 0.0) -> np.ndarray:
         """out [s][D] (or [s][len(cols)]) in double (steps a4 + a5, rank order)."""
-        gate, gate_s, up, up_s = _u8(gate), _f32(gate_s), _u8(up), _f32(up_s)
-        down, down_s, x = _u8(down), _f32(down_s), _f32(x).reshape(-1, D)
+        gate, gate_s, up, up_s = _u8(gate), _sc(fmt, gate_s), _u8(up), _sc(fmt, up_s)
+        down, down_s, x = _u8(down), _sc(fmt, down_s), _f32(x).reshape(-1, D)
         ids = np.ascontiguousarray(ids, dtype=np.int32)
         wts = _f32(wts)
         s = x.shape[0]
@@ -198,7 +209,7 @@ def default() -> Oracle:
 
 def __getattr__(name):
     # Module-level access to the default copy's methods: oracle.qgemv(...), ...
-    if name in {"threads", "packed_bytes", "codes", "e2m1", "code_value", "silu", "glu", "dequant_f32",
+    if name in {"threads", "packed_bytes", "codes", "e2m1", "code_value", "e8m0", "silu", "glu", "dequant_f32",
                 "qgemv", "qgemv_rows", "qgate_up", "qgate_up_rows", "expert_group"}:
         return getattr(default(), name)
     raise AttributeError(name)

@@ -20,8 +20,9 @@ from fractions import Fraction
 import numpy as np
 from scipy.special import expit
 
-from packing import (ALL_FMTS, INT3_G64, INT4_G, INT8_ROW, MXFP4_G32, dense, e2m1_table,
-                     group_of, load_table, pack, random_codes, values_of)
+from packing import (ALL_FMTS, INT3_G64, INT4_G, INT4_ROW, INT8_G, INT8_ROW, MXFP4_E8M0, MXFP4_G32, dense,
+                     draw_scales, e2m1_table, group_of, load_table, pack, random_codes, scale_values,
+                     to_stored_scales, values_of)
 
 
 def _close(a, b, rtol=1e-12, atol=0.0):
@@ -103,6 +104,40 @@ def pin_random_codes(orc):
         assert np.array_equal(got, codes), f"fmt {fmt}"
 
 
+def pin_e8m0(orc):
+    for b, v in load_table("e8m0_scales.txt"):
+        got = orc.e8m0(int(b))
+        if v == "nan":
+            assert np.isnan(got), b
+        else:
+            assert got == 2.0 ** int(v[2:]), (b, got, v)
+
+
+def pin_format_variants(orc):
+    """The three variant formats reduce to pinned ones: int4 with one scale per row is int4 with
+    a group of the whole row, int8 grouped with a group of the whole row is int8 per row, and
+    MXFP4 with ue8m0 byte 127 + k is MXFP4 with the f32 scale 2^k."""
+    rng = np.random.default_rng(41)
+    O, I, s = 3, 256, 2
+    x = rng.standard_normal((s, I)).astype(np.float32)
+    c4 = random_codes(INT4_ROW, O, I, rng)
+    sr = rng.lognormal(-4, 0.5, size=O).astype(np.float32)
+    assert np.array_equal(orc.qgemv(INT4_ROW, 0, pack(INT4_ROW, c4), sr, x, O, I),
+                          orc.qgemv(INT4_G, I, pack(INT4_G, c4), sr, x, O, I))
+    c8 = random_codes(INT8_G, O, I, rng)
+    assert np.array_equal(orc.qgemv(INT8_G, I, pack(INT8_G, c8), sr, x, O, I),
+                          orc.qgemv(INT8_ROW, 0, pack(INT8_ROW, c8), sr, x, O, I))
+    cm = random_codes(MXFP4_E8M0, O, I, rng)
+    k = rng.integers(-8, 3, size=O * (I // 32))
+    assert np.array_equal(orc.qgemv(MXFP4_E8M0, 0, pack(MXFP4_E8M0, cm), (127 + k).astype(np.uint8), x, O, I),
+                          orc.qgemv(MXFP4_G32, 0, pack(MXFP4_G32, cm), np.ldexp(1.0, k).astype(np.float32), x, O,
+                                    I))
+    # int8 grouped takes its groups along the row: groups of 32 with different scales
+    sg = rng.lognormal(-4, 0.5, size=O * (I // 32)).astype(np.float32)
+    want = x.astype(np.float64) @ (c8 * np.repeat(sg.reshape(O, -1).astype(np.float64), 32, axis=1)).T
+    _close(orc.qgemv(INT8_G, 32, pack(INT8_G, c8), sg, x, O, I), want)
+
+
 # --- step a2: f32 dequantized weights ----------------------------------------
 
 def pin_dequant_f32(orc):
@@ -111,24 +146,28 @@ def pin_dequant_f32(orc):
         for gs_req in (None, 64, 128):
             O, I = 3, 256
             gs = group_of(fmt, I, gs_req)
-            if fmt in (INT3_G64, MXFP4_G32, INT8_ROW) and gs_req is not None:
+            if fmt not in (INT4_G, INT8_G) and gs_req is not None:
                 continue
             codes = random_codes(fmt, O, I, rng)
-            scales = rng.lognormal(-4, 3.0, size=O * (I // gs)).astype(np.float32)
-            scales[0] = np.float32(1e-41)      # subnormal scale
-            scales[-1] = np.float32(1e36)       # large, no f32 overflow at |value| <= 128
+            scales = draw_scales(fmt, O * (I // gs), rng, -4, 3.0)
+            if fmt == MXFP4_E8M0:
+                scales[0], scales[-1] = 0, 250           # 2^-127 (subnormal in f32) and 2^123
+            else:
+                scales[0] = np.float32(1e-41)      # subnormal scale
+                scales[-1] = np.float32(1e36)       # large, no f32 overflow at |value| <= 128
             got = orc.dequant_f32(fmt, gs, pack(fmt, codes), scales, O, I)
-            want = values_of(fmt, codes).astype(np.float32) * np.repeat(scales.reshape(O, -1), gs, axis=1)
+            sv = scale_values(fmt, scales).astype(np.float32)    # exact: powers of two or f32 already
+            want = values_of(fmt, codes).astype(np.float32) * np.repeat(sv.reshape(O, -1), gs, axis=1)
             assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32)), f"fmt {fmt} gs {gs}"
 
 
 def pin_fixed_groups(orc):
-    """int3-g64 groups 64 inputs and MXFP4 32 whatever gs says; int8 one per row."""
+    """int3-g64 groups 64 inputs and MXFP4 32 whatever gs says; int8 and int4 per row one per row."""
     rng = np.random.default_rng(12)
-    for fmt, g in ((INT3_G64, 64), (MXFP4_G32, 32), (INT8_ROW, 256)):
+    for fmt, g in ((INT3_G64, 64), (MXFP4_G32, 32), (INT8_ROW, 256), (INT4_ROW, 256), (MXFP4_E8M0, 32)):
         O, I = 2, 256
         codes = random_codes(fmt, O, I, rng)
-        scales = rng.lognormal(-4, 1.0, size=O * (I // g)).astype(np.float32)
+        scales = draw_scales(fmt, O * (I // g), rng, -4, 1.0)
         a = orc.dequant_f32(fmt, g, pack(fmt, codes), scales, O, I)
         for other in (32, 64, 128):
             b = orc.dequant_f32(fmt, other, pack(fmt, codes), scales, O, I)
@@ -144,16 +183,16 @@ def pin_gemv_bruteforce(orc):
             for s in (1, 4):
                 O, I = 4, 64 if gs_req is None else 128
                 gs = group_of(fmt, I, gs_req)
-                if gs_req is not None and fmt != INT4_G:
+                if gs_req is not None and fmt not in (INT4_G, INT8_G):
                     continue
                 codes = random_codes(fmt, O, I, rng)
-                scales = rng.lognormal(-4, 0.5, size=O * (I // gs)).astype(np.float32)
+                scales = draw_scales(fmt, O * (I // gs), rng)
                 x = rng.standard_normal((s, I)).astype(np.float32)
                 got = orc.qgemv(fmt, gs, pack(fmt, codes), scales, x, O, I)
                 want = x.astype(np.float64) @ dense(fmt, codes, scales, gs).T
                 _close(got, want)
                 # scale 1: a plain dense matvec of the code values
-                ones = np.ones(O * (I // gs), dtype=np.float32)
+                ones = to_stored_scales(fmt, np.ones(O * (I // gs)))
                 got1 = orc.qgemv(fmt, gs, pack(fmt, codes), ones, x, O, I)
                 _close(got1, x.astype(np.float64) @ values_of(fmt, codes).T)
                 rows = np.array([3, 0, 2])
@@ -163,6 +202,8 @@ def pin_gemv_bruteforce(orc):
 def pin_zero_scales(orc):
     rng = np.random.default_rng(17)
     for fmt in ALL_FMTS:
+        if fmt == MXFP4_E8M0:
+            continue                                 # ue8m0 has no zero
         O, I = 3, 128
         gs = group_of(fmt, I)
         codes = random_codes(fmt, O, I, rng)
@@ -170,7 +211,7 @@ def pin_zero_scales(orc):
         zero = np.zeros(O * (I // gs), dtype=np.float32)
         assert not orc.qgemv(fmt, gs, pack(fmt, codes), zero, x, O, I).any()
         if gs < I:
-            scales = rng.lognormal(-4, 0.5, size=O * (I // gs)).astype(np.float32)
+            scales = draw_scales(fmt, O * (I // gs), rng)
             scales.reshape(O, -1)[:, 1] = 0.0        # group 1 of every row is zero
             y1 = orc.qgemv(fmt, gs, pack(fmt, codes), scales, x, O, I)
             codes2 = codes.copy()
@@ -185,7 +226,7 @@ def pin_linearity(orc):
         O, I = 4, 128
         gs = group_of(fmt, I)
         w = pack(fmt, random_codes(fmt, O, I, rng))
-        scales = rng.lognormal(-4, 0.5, size=O * (I // gs)).astype(np.float32)
+        scales = draw_scales(fmt, O * (I // gs), rng)
         x1 = rng.standard_normal(I).astype(np.float32)
         x2 = rng.standard_normal(I).astype(np.float32)
         x1[1::2] = 0.0                              # disjoint supports: a*x1 + b*x2 exact in f32
@@ -205,7 +246,7 @@ def pin_integer_exact(orc):
         gs = group_of(fmt, I)
         codes = random_codes(fmt, O, I, rng)
         k = rng.integers(-8, 1, size=O * (I // gs))
-        scales = np.ldexp(np.ones(k.size), k).astype(np.float32)
+        scales = to_stored_scales(fmt, np.ldexp(np.ones(k.size), k))
         x = rng.integers(-4, 5, size=(2, I)).astype(np.float32)
         got = orc.qgemv(fmt, gs, pack(fmt, codes), scales, x, O, I)
         vals = values_of(fmt, codes)
@@ -232,8 +273,8 @@ def pin_gate_up(orc):
         F, D, s = 8, 128, 2
         gs = group_of(fmt, D)
         cg, cu = random_codes(fmt, F, D, rng), random_codes(fmt, F, D, rng)
-        sg = rng.lognormal(-4, 0.5, size=F * (D // gs)).astype(np.float32)
-        su = rng.lognormal(-4, 0.5, size=F * (D // gs)).astype(np.float32)
+        sg = draw_scales(fmt, F * (D // gs), rng)
+        su = draw_scales(fmt, F * (D // gs), rng)
         x = rng.standard_normal((s, D)).astype(np.float32)
         got = orc.qgate_up(fmt, gs, pack(fmt, cg), sg, pack(fmt, cu), su, x, F, D)
         g = x.astype(np.float64) @ dense(fmt, cg, sg, gs).T
@@ -276,8 +317,8 @@ def pin_gate_up_clamped(orc):
         F, D, s = 8, 128, 2
         gs = group_of(fmt, D)
         cg, cu = random_codes(fmt, F, D, rng), random_codes(fmt, F, D, rng)
-        sg = rng.lognormal(-3, 0.5, size=F * (D // gs)).astype(np.float32)
-        su = rng.lognormal(-3, 0.5, size=F * (D // gs)).astype(np.float32)
+        sg = draw_scales(fmt, F * (D // gs), rng, -3)
+        su = draw_scales(fmt, F * (D // gs), rng, -3)
         x = rng.standard_normal((s, D)).astype(np.float32)
         g = x.astype(np.float64) @ dense(fmt, cg, sg, gs).T
         u = x.astype(np.float64) @ dense(fmt, cu, su, gs).T
@@ -295,9 +336,9 @@ def _expert_store(fmt, E, D, F, rng):
     cg = [random_codes(fmt, F, D, rng) for _ in range(E)]
     cu = [random_codes(fmt, F, D, rng) for _ in range(E)]
     cd = [random_codes(fmt, D, F, rng) for _ in range(E)]
-    sg = [rng.lognormal(-4, 0.5, size=F * (D // gs_gu)).astype(np.float32) for _ in range(E)]
-    su = [rng.lognormal(-4, 0.5, size=F * (D // gs_gu)).astype(np.float32) for _ in range(E)]
-    sd = [rng.lognormal(-4, 0.5, size=D * (F // gs_dn)).astype(np.float32) for _ in range(E)]
+    sg = [draw_scales(fmt, F * (D // gs_gu), rng) for _ in range(E)]
+    su = [draw_scales(fmt, F * (D // gs_gu), rng) for _ in range(E)]
+    sd = [draw_scales(fmt, D * (F // gs_dn), rng) for _ in range(E)]
     packed = (np.concatenate([pack(fmt, c) for c in cg]), np.concatenate(sg),
               np.concatenate([pack(fmt, c) for c in cu]), np.concatenate(su),
               np.concatenate([pack(fmt, c) for c in cd]), np.concatenate(sd))
@@ -350,6 +391,7 @@ def pin_expert_group(orc):
         assert not orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, wts, act=1, limit=0.0).any()
 
 
-ALL_PINS = [pin_e2m1, pin_int4_nibbles, pin_int3_planes, pin_int8_bytes, pin_random_codes,
+ALL_PINS = [pin_e2m1, pin_e8m0, pin_int4_nibbles, pin_int3_planes, pin_int8_bytes, pin_random_codes,
+            pin_format_variants,
             pin_dequant_f32, pin_fixed_groups, pin_gemv_bruteforce, pin_zero_scales, pin_linearity,
             pin_integer_exact, pin_silu, pin_clamped_glu, pin_gate_up, pin_gate_up_clamped, pin_expert_group]

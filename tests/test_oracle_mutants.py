@@ -25,7 +25,7 @@ MUTANTS = {
     "e2m1_subnormal": ("(e == 0) ? 0.5 * m", "(e == 0) ? 1.0 * m"),
     "scale_first_group_only": ("scales[o * (I / gs) + i / gs]", "scales[o * (I / gs)]"),
     "int3_group_32": ("case ORACLE_INT3_G64: return 64;", "case ORACLE_INT3_G64: return 32;"),
-    "mxfp4_group_64": ("case ORACLE_MXFP4_G32: return 32;", "case ORACLE_MXFP4_G32: return 64;"),
+    "mxfp4_group_64": ("case ORACLE_MXFP4_E8M0: return 32;", "case ORACLE_MXFP4_E8M0: return 64;"),
     "scale_group_mod": ("scales[o * (I / gs) + i / gs]", "scales[o * (I / gs) + i % (I / gs)]"),
     "gemv_dropped_term": ("for (long i = 0; i < I; i++)\n        acc +=", "for (long i = 1; i < I; i++)\n        acc +="),
     "gemv_token_ignored": ("y[t * O + o] = row_dot(fmt, gs, w, scales, O, I, o, x + t * I);",
@@ -37,6 +37,12 @@ MUTANTS = {
     "clamp_gate_both_sides": ("if (g > limit) g = limit;", "if (g > limit) g = limit;\n        if (g < -limit) g = -limit;"),
     "router_weight_dropped": ("out[t * ncols + j] += wr * z;", "out[t * ncols + j] += z;"),
     "down_transposed": ("oracle_weight(fmt, gs, de, dse, D, F, d, f)", "oracle_weight(fmt, gs, de, dse, F, D, f, d)"),
+    "e8m0_bias": ("ldexp(1.0, e - 127)", "ldexp(1.0, e - 128)"),
+    "e8m0_scales_as_f32": ("if (fmt == ORACLE_MXFP4_E8M0)\n        return", "if (fmt == -1)\n        return"),
+    "int8_grouped_per_row": ("case ORACLE_INT8_ROW:\n    case ORACLE_INT4_ROW: return I;",
+                             "case ORACLE_INT8_ROW:\n    case ORACLE_INT8_G:\n    case ORACLE_INT4_ROW: return I;"),
+    "int4_row_no_offset": ("case ORACLE_INT4_ROW:\n    case ORACLE_INT4_G: return (double)(code - 8);",
+                           "case ORACLE_INT4_G: return (double)(code - 8);\n    case ORACLE_INT4_ROW: return (double)code;"),
     "expert_rank_last_only": ("out[t * ncols + j] = 0.0;", "out[t * ncols + j] = 0.0 * out[t * ncols + j];"),
 }
 
