@@ -41,7 +41,9 @@ METRIC = "achieved weight-stream GB/s (% of GB300 HBM peak); µs per fused exper
 DEFAULT_WORKLOAD = "int4_g32_16384x6144_s1"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-FMT_LABEL = {1: "int8-row", 4: "int4-g", 5: "int3-g64", 7: "mxfp4-g32"}
+FMT_LABEL = {1: "int8-row", 2: "int4-row", 4: "int4-g", 5: "int3-g64", 7: "mxfp4-g32", 8: "mxfp4-e8m0-g32",
+             13: "int8-g"}
+GROUPED = (synth.INT4_G, synth.INT8_G)   # formats whose group size the caller passes
 
 
 # ---------------------------------------------------------------------------
@@ -191,7 +193,7 @@ class GemvBench:
         self.x_host = wl.x()
         self.x = torch.from_numpy(self.x_host).to(device)
         self.y = torch.empty(wl.s, wl.O, dtype=torch.float32, device=device)
-        self.gs = wl.gs if wl.fmt == synth.INT4_G else 0
+        self.gs = wl.gs if wl.fmt in GROUPED else 0
         self.launches_per_step = 1
         self.l2_note = f"rotates {self.ncopies} weight copies ({self.ncopies * self.step_bytes / 1e6:.0f} MB > 2x L2)"
 
@@ -237,7 +239,8 @@ class ExpertBench:
         for name, which in wl.MATRICES:
             nb, ns = wl.sizes(which)
             self.d[name] = torch.empty(wl.E * nb, dtype=torch.uint8, device=device)
-            self.d[name + "_s"] = torch.empty(wl.E * ns, dtype=torch.float32, device=device)
+            self.d[name + "_s"] = torch.empty(wl.E * ns, dtype=torch.uint8 if wl.fmt == synth.MXFP4_E8M0
+                                              else torch.float32, device=device)
 
         def sink(name, slot, w, sc):
             self.d[name][slot * w.size:(slot + 1) * w.size].copy_(torch.from_numpy(w))
@@ -262,7 +265,7 @@ class ExpertBench:
         self.ws_bytes = qexpert_group_workspace(wl.E, wl.D, wl.F, wl.s, wl.k)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.gs = wl.gs if wl.fmt == synth.INT4_G else 0
+        self.gs = wl.gs if wl.fmt in GROUPED else 0
         self.expert_bytes = wl.expert_bytes()
         self.route_bytes = [len(np.unique(self.ids_host[r])) * self.expert_bytes for r in range(self.nroutes)]
         self.launches_per_step = 4
@@ -340,7 +343,7 @@ def oracle_sample_runner(wl, target_s: float, swiglu_limit=None):
     ids, _ = wl.routing(step=0)
     x = wl.x(step=0)[:1]
     st = wl.store(ids[0, :1])
-    per_row = 2 * (synth.packed_bytes(wl.fmt, 1, wl.D) + 4 * (wl.D // wl.gs))
+    per_row = 2 * (synth.packed_bytes(wl.fmt, 1, wl.D) + synth.scale_itemsize(wl.fmt) * (wl.D // wl.gs))
 
     def run_rows(nrows, start=0):
         rows = (np.arange(nrows) + start) % wl.F
@@ -399,18 +402,35 @@ def reference_arm(args, wl, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def gemv_kernel_name(wl):
-    """The kernel one qgemv call of this workload runs (the library's automatic choice)."""
-    return "k_stream" if (wl.s == 1 and wl.fmt != 5) else "k_tile"
+def gemv_kernel_name(wl, sms=152):
+    """The kernel one qgemv call of this workload runs (the library's automatic choice):
+    the tile kernel for int3 and several activation rows, and for one row when
+    lanes share scales (per-row scales, ue8m0 words, groups longer than a
+    chunk) on a matrix with at least 64 rows per SM and a tile plan that fits."""
+    if wl.s > 1 or wl.fmt == synth.INT3_G64:
+        return "k_tile"
+    int8 = wl.fmt in (synth.INT8_ROW, synth.INT8_G)
+    codes_per_chunk, codes_per_slice = (16, 512) if int8 else (32, 1024)
+    if wl.fmt in (synth.INT8_ROW, synth.INT4_ROW):
+        shares, fits = True, True
+    elif wl.fmt == synth.MXFP4_E8M0:
+        shares, fits = True, wl.I % 512 == 0
+    elif wl.fmt in GROUPED:
+        shares = wl.gs > codes_per_chunk
+        fits = codes_per_slice % wl.gs == 0 and 4 * codes_per_slice // wl.gs >= 16 and (4 * wl.I // wl.gs) % 16 == 0
+    else:
+        shares, fits = False, False
+    short = -(-wl.O // sms) < 64
+    return "k_tile" if (shares and fits and not short) else "k_stream"
 
 
 def gemv_config(wl):
-    return {"workload": wl.name, "kind": "qgemv", "fmt": FMT_LABEL[wl.fmt] + (str(wl.gs) if wl.fmt == 4 else ""),
+    return {"workload": wl.name, "kind": "qgemv", "fmt": FMT_LABEL[wl.fmt] + (str(wl.gs) if wl.fmt in GROUPED else ""),
             "O": wl.O, "I": wl.I, "s": wl.s, "gs": wl.gs, "parallelism": "replicas"}
 
 
 def expert_config(wl):
-    return {"workload": wl.name, "kind": "qexpert_group", "fmt": FMT_LABEL[wl.fmt] + (str(wl.gs) if wl.fmt == 4 else ""),
+    return {"workload": wl.name, "kind": "qexpert_group", "fmt": FMT_LABEL[wl.fmt] + (str(wl.gs) if wl.fmt in GROUPED else ""),
             "E": wl.E, "D": wl.D, "F": wl.F, "s": wl.s, "k": wl.k, "gs": wl.gs, "parallelism": "replicas"}
 
 
@@ -422,7 +442,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS + synth.VARIANT_WORKLOADS)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph-len", type=int, default=64, help="calls captured per CUDA graph replay")

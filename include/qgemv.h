@@ -47,9 +47,19 @@
  *                      per byte); value = code - 4; gs must be 0 or 64.
  *      QFMT_MXFP4_G32  [O][I/2] bytes of e2m1 nibbles, the low nibble holds the
  *                      even input; gs must be 0 or 32.
+ *    Variants that share those decoders (colibri's other storage ids):
+ *      QFMT_INT4_ROW   the int4 layout with one scale per row (gs 0 or I).
+ *      QFMT_INT8_G     the int8 layout with one scale per group; gs a power of
+ *                      two in [16, 512].
+ *      QFMT_MXFP4_E8M0 the MXFP4 layout with the checkpoint's scale bytes as
+ *                      stored: `scales` points to uint8 ue8m0 bytes [O][I/32]
+ *                      (value 2^(e - 127); e = 255 is NaN), read in place of
+ *                      the host-expanded f32; gs must be 0 or 32.
  *  - Alignment: packed weights and activation/hidden vectors (x, h, workspace)
- *    16-byte aligned; scales and outputs 4-byte aligned; else QSTATUS_MISALIGNED.
- *  - Sizes: I % 16 == 0 (int8), I % gs == 0 (grouped formats), O, I, s >= 1.
+ *    16-byte aligned; scales and outputs 4-byte aligned (ue8m0 scale bytes
+ *    too); else QSTATUS_MISALIGNED.
+ *  - Sizes: I % 16 == 0 (int8), I % 32 == 0 (int4 per row), I % 128 == 0
+ *    (MXFP4 with ue8m0 bytes), I % gs == 0 (grouped formats), O, I, s >= 1.
  *    The activation rows of one launch share shared memory with the weight
  *    copy rings, so a row of I f32 must fit what the rings leave: I up to
  *    about 37,000 (int8, int4, MXFP4; qgate_up and qexpert_group too) or
@@ -68,9 +78,12 @@ extern "C" {
 /* Weight formats (colibri's storage ids). */
 enum {
     QFMT_INT8_ROW = 1,
+    QFMT_INT4_ROW = 2,
     QFMT_INT4_G = 4,
     QFMT_INT3_G64 = 5,
-    QFMT_MXFP4_G32 = 7
+    QFMT_MXFP4_G32 = 7,
+    QFMT_MXFP4_E8M0 = 8,
+    QFMT_INT8_G = 13
 };
 
 /* Status codes. */
@@ -101,7 +114,7 @@ enum {
 /*
  * y[t][o] = sum_i value(W[o][i]) * scales[o][i/gs] * x[t][i],  t < s, o < O.
  *   w       packed weights (layout above)
- *   scales  f32 [O][I/gs]
+ *   scales  f32 [O][I/gs] (QFMT_MXFP4_E8M0: uint8 [O][I/32])
  *   x       f32 [s][I]
  *   y       f32 [s][O], written
  * Weights are streamed once per group of up to 8 activation rows; larger s is
@@ -135,7 +148,8 @@ size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
  *   e = ids[t][r], summed in rank order r for every t.
  *   gate, up  packed [E][F][D] (expert e's F x D matrix at e * its size),
  *             scales f32 [E][F][D/gs]
- *   down      packed [E][D][F], scales f32 [E][D][F/gs]   (int8: one per row)
+ *   down      packed [E][D][F], scales f32 [E][D][F/gs]   (row formats: one per row;
+ *             QFMT_MXFP4_E8M0: the scales are ue8m0 bytes of the same counts)
  *   x         f32 [s][D];  ids int32 [s][k];  wts f32 [s][k]
  *   out       f32 [s][D], written
  *   workspace device scratch of ws_bytes >= qexpert_group_workspace(E, D, F, s, k)

@@ -7,6 +7,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 INT8_ROW, INT4_G, INT3_G64, MXFP4_G32 = 1, 4, 5, 7
+INT4_ROW, MXFP4_E8M0, INT8_G = 2, 8, 13
 GATE = 1e-3      # max_o |y - y*| / max_o |y*| per output vector, from the workloads' statement
 
 
@@ -41,9 +42,9 @@ def max_rel(y, ystar) -> float:
 def packed_rows(fmt: int, w: np.ndarray, O: int, I: int, rows) -> np.ndarray:
     """The packed bytes of the given rows, as a len(rows) x I matrix of format fmt."""
     rows = np.asarray(rows)
-    if fmt == INT8_ROW:
+    if fmt in (INT8_ROW, INT8_G):
         return w.reshape(O, I)[rows].reshape(-1)
-    if fmt in (INT4_G, MXFP4_G32):
+    if fmt in (INT4_G, INT4_ROW, MXFP4_G32, MXFP4_E8M0):
         return w.reshape(O, I // 2)[rows].reshape(-1)
     A = w[: O * I // 4].reshape(O, I // 4)[rows]
     B = w[O * I // 4:].reshape(O, I // 8)[rows]

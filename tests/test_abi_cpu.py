@@ -49,7 +49,17 @@ A = 1 << 20
 
 
 @pytest.mark.parametrize("fmt,gs,I,want", [
-    (2, 32, 1024, -1),          # unknown format
+    (3, 32, 1024, -1),          # unknown format
+    (6, 0, 1024, -1),           # unknown format
+    (2, 32, 1024, -1),          # int4 per row: gs must be 0 or I
+    (2, 0, 1040, -2),           # int4 per row: I not a multiple of 32
+    (13, 8, 1024, -1),          # int8 grouped: group below 16
+    (13, 48, 1024, -1),         # int8 grouped: group not a power of two
+    (13, 0, 1024, -1),          # int8 grouped: a group size is required
+    (13, 1024, 2048, -1),       # int8 grouped: group above 512
+    (13, 64, 1040, -2),         # int8 grouped: I not a multiple of gs
+    (8, 64, 1024, -1),          # MXFP4 with ue8m0 bytes is group 32 only
+    (8, 0, 1056, -2),           # ue8m0 bytes: I not a multiple of 128
     (4, 48, 1024, -1),          # int4 group size not a power of two
     (4, 16, 1024, -1),          # int4 group below 32
     (5, 32, 1024, -1),          # int3 is group 64 only

@@ -22,7 +22,8 @@ def small_store(fmt, E, D, F, seed):
     m = {}
     for name, (O, I, g) in {"gate": (F, D, gs_up), "up": (F, D, gs_up), "down": (D, F, gs_dn)}.items():
         m[name] = np.concatenate([synth.draw_packed(fmt, O, I, rng) for _ in range(E)])
-        m[name + "_s"] = np.concatenate([synth.draw_scales(O, I, g, rng, "lognormal", -4.0) for _ in range(E)])
+        m[name + "_s"] = np.concatenate([synth.draw_scales(O, I, g, rng, "lognormal", -4.0, fmt=fmt)
+                                         for _ in range(E)])
     return m
 
 
@@ -99,7 +100,8 @@ def full_store_on_device(wl):
     for name, which in wl.MATRICES:
         nb, ns = wl.sizes(which)
         d[name] = torch.empty(wl.E * nb, dtype=torch.uint8, device=cuda())
-        d[name + "_s"] = torch.empty(wl.E * ns, dtype=torch.float32, device=cuda())
+        d[name + "_s"] = torch.empty(wl.E * ns, dtype=torch.uint8 if wl.fmt == synth.MXFP4_E8M0 else torch.float32,
+                                     device=cuda())
 
     def sink(name, slot, w, sc):
         d[name][slot * w.size:(slot + 1) * w.size].copy_(torch.from_numpy(w))

@@ -14,6 +14,7 @@ import os
 from . import _build
 
 QFMT_INT8_ROW, QFMT_INT4_G, QFMT_INT3_G64, QFMT_MXFP4_G32 = 1, 4, 5, 7
+QFMT_INT4_ROW, QFMT_MXFP4_E8M0, QFMT_INT8_G = 2, 8, 13
 
 QSTATUS = {
     0: "QSTATUS_OK",

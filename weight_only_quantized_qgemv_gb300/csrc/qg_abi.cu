@@ -48,6 +48,16 @@ static int check_fmt(int fmt, int gs, int I, int* gs_out)
         if (I % 16) return QSTATUS_BAD_DIM;
         *gs_out = I;
         return QSTATUS_OK;
+    case QFMT_INT8_G:   // a warp step covers 512 codes: at most one group per step
+        if (gs < 16 || gs > 512 || (gs & (gs - 1))) return QSTATUS_BAD_FMT;
+        if (I % gs) return QSTATUS_BAD_DIM;
+        *gs_out = gs;
+        return QSTATUS_OK;
+    case QFMT_INT4_ROW:
+        if (gs != 0 && gs != I) return QSTATUS_BAD_FMT;
+        if (I % 32) return QSTATUS_BAD_DIM;
+        *gs_out = I;
+        return QSTATUS_OK;
     case QFMT_INT4_G:
         if (gs < 32 || gs > 1024 || (gs & (gs - 1))) return QSTATUS_BAD_FMT;
         if (I % gs) return QSTATUS_BAD_DIM;
@@ -61,6 +71,11 @@ static int check_fmt(int fmt, int gs, int I, int* gs_out)
     case QFMT_MXFP4_G32:
         if (gs != 0 && gs != 32) return QSTATUS_BAD_FMT;
         if (I % 32) return QSTATUS_BAD_DIM;
+        *gs_out = 32;
+        return QSTATUS_OK;
+    case QFMT_MXFP4_E8M0:   // four lanes read their scale bytes as one aligned word
+        if (gs != 0 && gs != 32) return QSTATUS_BAD_FMT;
+        if (I % 128) return QSTATUS_BAD_DIM;
         *gs_out = 32;
         return QSTATUS_OK;
     default:
@@ -85,8 +100,11 @@ static size_t ring_bytes(int fmt, int nm)
 {
     switch (fmt) {
     case QFMT_INT8_ROW: return ring_bytes_int8(nm);
+    case QFMT_INT8_G: return ring_bytes_int8g(nm);
+    case QFMT_INT4_ROW: return ring_bytes_int4r(nm);
     case QFMT_INT4_G: return ring_bytes_int4(nm);
     case QFMT_INT3_G64: return ring_bytes_int3(nm);
+    case QFMT_MXFP4_E8M0: return ring_bytes_mxfp4e(nm);
     default: return ring_bytes_mxfp4(nm);
     }
 }
@@ -102,8 +120,11 @@ static int rows_per_launch(int fmt, int nm, int I)
 #define QG_FMT_SWITCH(fmt, CALL)                                 \
     switch (fmt) {                                               \
     case QFMT_INT8_ROW: e = CALL(int8); break;                   \
+    case QFMT_INT8_G: e = CALL(int8g); break;                    \
+    case QFMT_INT4_ROW: e = CALL(int4r); break;                  \
     case QFMT_INT4_G: e = CALL(int4); break;                     \
     case QFMT_INT3_G64: e = CALL(int3); break;                   \
+    case QFMT_MXFP4_E8M0: e = CALL(mxfp4e); break;               \
     default: e = CALL(mxfp4); break;                             \
     }
 
@@ -306,8 +327,9 @@ int qkernel_policy(int policy)
 
 int qdevice_error(int clear)
 {
-    const int e[4] = {device_error_int8(clear), device_error_int4(clear), device_error_int3(clear),
-                      device_error_mxfp4(clear)};
+    const int e[7] = {device_error_int8(clear),  device_error_int8g(clear), device_error_int4r(clear),
+                      device_error_int4(clear),  device_error_int3(clear),  device_error_mxfp4(clear),
+                      device_error_mxfp4e(clear)};
     for (int v : e)
         if (v != QSTATUS_OK) return v;
     return QSTATUS_OK;
@@ -428,13 +450,16 @@ int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, co
     int r_up = 1, r_dn = 1;
     switch (fmt) {
     case QFMT_INT8_ROW: r_up = tile_rows_int8(2); r_dn = tile_rows_int8(1); break;
+    case QFMT_INT8_G: r_up = tile_rows_int8g(2); r_dn = tile_rows_int8g(1); break;
+    case QFMT_INT4_ROW: r_up = tile_rows_int4r(2); r_dn = tile_rows_int4r(1); break;
     case QFMT_INT4_G: r_up = tile_rows_int4(2); r_dn = tile_rows_int4(1); break;
     case QFMT_INT3_G64: r_up = tile_rows_int3(2); r_dn = tile_rows_int3(1); break;
+    case QFMT_MXFP4_E8M0: r_up = tile_rows_mxfp4e(2); r_dn = tile_rows_mxfp4e(1); break;
     default: r_up = tile_rows_mxfp4(2); r_dn = tile_rows_mxfp4(1); break;
     }
     a.tpb_up = (F + r_up - 1) / r_up;
     a.tpb_down = (D + r_dn - 1) / r_dn;
-    a.gs = fmt == QFMT_INT8_ROW ? 0 : g_up;
+    a.gs = (fmt == QFMT_INT8_ROW || fmt == QFMT_INT4_ROW) ? 0 : g_up;   // per-row formats: one scale per row
     a.gate = gate; a.up = up; a.down = down;
     a.gate_s = gate_s; a.up_s = up_s; a.down_s = down_s;
     a.E = E; a.D = D; a.F = F; a.s = s; a.k = k;

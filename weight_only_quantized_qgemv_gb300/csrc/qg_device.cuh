@@ -35,7 +35,25 @@
 
 namespace qg {
 
-enum : int { FMT_INT8_ROW = 1, FMT_INT4_G = 4, FMT_INT3_G64 = 5, FMT_MXFP4_G32 = 7 };
+enum : int {
+    FMT_INT8_ROW = 1, FMT_INT4_ROW = 2, FMT_INT4_G = 4, FMT_INT3_G64 = 5, FMT_MXFP4_G32 = 7, FMT_MXFP4_E8M0 = 8,
+    FMT_INT8_G = 13
+};
+
+// A format is a code decoding (int8, int4, int3 or e2m1: the first four ids
+// above) and a scale kind: one f32 per row, f32 per group, or one ue8m0 byte
+// per group of 32.
+enum : int { SK_ROW = 0, SK_F32 = 1, SK_E8M0 = 2 };
+__host__ __device__ constexpr int decode_of(int f)
+{
+    return f == FMT_INT8_G ? FMT_INT8_ROW
+         : f == FMT_INT4_ROW ? FMT_INT4_G
+         : f == FMT_MXFP4_E8M0 ? FMT_MXFP4_G32 : f;
+}
+__host__ __device__ constexpr int scale_kind_of(int f)
+{
+    return (f == FMT_INT8_ROW || f == FMT_INT4_ROW) ? SK_ROW : (f == FMT_MXFP4_E8M0 ? SK_E8M0 : SK_F32);
+}
 
 // Elements a lane decodes per chunk.
 template <int FMT> struct Traits;
@@ -124,31 +142,49 @@ __device__ __forceinline__ float ldg_f32(const float* p)
 // ---------------------------------------------------------------------------
 struct Mat {
     const uint8_t* w;      // packed codes (int3: plane A, then plane B)
-    const float* sc;       // scales [O][I/gs]
+    const float* sc;       // scales [O][I/gs] (ue8m0: bytes, addressed through sc_ptr)
     long long O;           // rows
     int I;                 // inputs per row
-    int ngrp;              // scale groups per row (I/gs; int8: 1)
-    int gsh;               // chunk -> group shift (int4: log2(gs/32)); else 0
+    int ngrp;              // scale groups per row (I/gs; per-row formats: 1)
+    int gsh;               // chunk -> group shift: log2(gs / inputs per chunk); per-row formats: 0
 };
+
+// Scale element n of a scale array: f32 elements, or bytes for ue8m0.
+template <int SK>
+__host__ __device__ __forceinline__ const float* sc_ptr(const float* base, long long n)
+{
+    if constexpr (SK == SK_E8M0) return reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(base) + n);
+    else return base + n;
+}
+
+// ue8m0 byte -> f32: 2^(e - 127) is the byte in the exponent field; byte 0 is
+// the subnormal 2^-127 and byte 255 NaN (both get mantissa bit 22).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e)
+{
+    return __uint_as_float((e << 23) | ((e == 0u || e == 255u) ? 0x00400000u : 0u));
+}
 
 template <int FMT> struct Chunk { uint4 w; };
 template <> struct Chunk<FMT_INT3_G64> { uint4 a; uint2 b; };
 
-template <int FMT>
-__device__ __forceinline__ void load_chunk(const Mat& m, long long o, int q, Chunk<FMT>& c, float& sc)
+// One chunk of row o and its scale, straight from global memory (the
+// dequantization kernel).  QF is the full format.
+template <int QF>
+__device__ __forceinline__ void load_chunk(const Mat& m, long long o, int q, Chunk<decode_of(QF)>& c, float& sc)
 {
+    constexpr int FMT = decode_of(QF), SK = scale_kind_of(QF);
     if constexpr (FMT == FMT_INT8_ROW) {
         c.w = ldg_stream16(m.w + o * m.I + (long long)q * 16);
-        sc = ldg_f32(m.sc + o);
     } else if constexpr (FMT == FMT_INT3_G64) {
         const long long rowA = (long long)(m.I / 4), rowB = (long long)(m.I / 8);
         c.a = ldg_stream16(m.w + o * rowA + (long long)q * 16);
         c.b = ldg_stream8(m.w + m.O * rowA + o * rowB + (long long)q * 8);
-        sc = ldg_f32(m.sc + o * m.ngrp + q);
     } else {
         c.w = ldg_stream16(m.w + o * (long long)(m.I / 2) + (long long)q * 16);
-        sc = ldg_f32(m.sc + o * m.ngrp + (q >> m.gsh));
     }
+    const long long n = o * m.ngrp + (SK == SK_ROW ? 0 : (q >> m.gsh));
+    if constexpr (SK == SK_E8M0) sc = e8m0_to_f32(reinterpret_cast<const uint8_t*>(m.sc)[n]);
+    else sc = ldg_f32(m.sc + n);
 }
 
 #ifndef QG_INT3_SPREAD
@@ -618,6 +654,14 @@ __device__ __forceinline__ uint2 lds8(uint32_t a)
     return v;
 #endif
 }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a)
+{
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(qg_smem4) + a);
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a)
+{
+    return *reinterpret_cast<const uint8_t*>(reinterpret_cast<const char*>(qg_smem4) + a);
+}
 __device__ __forceinline__ float lds_f32(uint32_t a)
 {
 #if QG_CXX_LDS
@@ -717,8 +761,13 @@ __host__ __device__ constexpr int ring_slot_bytes()
 // once per finished tile from every lane: sink(value, index, lane_holds_it,
 // first row of the tile, row_end) with index v = (s * R + r) * NM + m.
 // ---------------------------------------------------------------------------
-template <int FMT, int S, int R, int P, int NM, bool LOOP_S = false>
+// SH: lanes share scales (one per row, ue8m0 words, or groups longer than a
+// chunk): only the first lane of each sharing set copies a scale (word) and
+// the others take it by shuffle -- many lanes copying one address are slow.
+template <int QF, int S, int R, int P, int NM, bool LOOP_S = false, bool SH = false>
 struct RowStreamer {
+    static constexpr int FMT = decode_of(QF);       // how codes decode
+    static constexpr int SK = scale_kind_of(QF);    // how scales are stored
     static constexpr int EPL = Traits<FMT>::EPL;
     static constexpr int NR = NM * R;
     static constexpr int V = pow2_ceil(S * R * NM);
@@ -728,8 +777,9 @@ struct RowStreamer {
 
     const uint8_t* wp[NR];    // this lane's next chunk of each row (int3: plane A)
     const uint8_t* bp[NR];    // int3 plane B
-    const float* sp[NR];      // this lane's next scale of each row
+    const float* sp[NR];      // this lane's next scale of each row (ue8m0: the aligned word holding it)
     int sstep;                // scale advance per step
+    uint32_t lead;            // SH: this lane minus the first lane sharing its scale (word), which copies it
     uint32_t ring;            // this lane's byte offset in slot 0 of the warp's ring
     uint32_t sbase;           // shared-window address of the dynamic shared memory
 
@@ -759,15 +809,15 @@ struct RowStreamer {
                 const int rr = m * R + r;
                 if constexpr (FMT == FMT_INT8_ROW) {
                     wp[rr] = M.w + o * M.I + lane * 16;
-                    sp[rr] = M.sc + o;
                 } else if constexpr (FMT == FMT_INT3_G64) {
                     wp[rr] = M.w + o * (long long)(M.I / 4) + lane * 16;
                     bp[rr] = M.w + M.O * (long long)(M.I / 4) + o * (long long)(M.I / 8) + lane * 8;
-                    sp[rr] = M.sc + o * M.ngrp + lane;
                 } else {
                     wp[rr] = M.w + o * (long long)(M.I / 2) + lane * 16;
-                    sp[rr] = M.sc + o * M.ngrp + (lane >> M.gsh);
                 }
+                if constexpr (SK == SK_ROW) sp[rr] = M.sc + o;
+                else if constexpr (SK == SK_E8M0) sp[rr] = sc_ptr<SK>(M.sc, o * M.ngrp + (lane & ~3));
+                else sp[rr] = M.sc + o * M.ngrp + (lane >> M.gsh);
             }
         }
     }
@@ -784,11 +834,12 @@ struct RowStreamer {
                 if (ok && (rr % R) < it_valid) {
                     cp_async16(slot + rr * 512, wp[rr]);
                     if constexpr (FMT == FMT_INT3_G64) cp_async8(slot + B_OFF + rr * 256 - lane * 8, bp[rr]);
-                    cp_async4(slot + S_OFF + rr * 128 - lane * 12, sp[rr]);
+                    // one copy per scale (word): many lanes copying one address are slow
+                    if (!SH || lead == 0) cp_async4(slot + S_OFF + rr * 128 - lane * 12, sp[rr]);
                 }
                 wp[rr] += 512;
                 if constexpr (FMT == FMT_INT3_G64) bp[rr] += 256;
-                sp[rr] += sstep;
+                sp[rr] = sc_ptr<SK>(sp[rr], sstep);
             }
             ++issued;
             if (++it_c == nsteps) {
@@ -815,8 +866,10 @@ struct RowStreamer {
         sbase = smem_base();
         nchunks = m[0].I / EPL;
         nsteps = (nchunks + 31) / 32;
-        // int8: one scale per row; int4: 32 chunks span 32 >> gsh groups
-        sstep = FMT == FMT_INT8_ROW ? 0 : (32 >> m[0].gsh);
+        // one scale per row: none; else 32 chunks span 32 >> gsh groups (ue8m0: that many bytes)
+        sstep = SK == SK_ROW ? 0 : (32 >> m[0].gsh);
+        // lanes sharing a scale: all 32 (one per row), 2^gsh (a group spans 2^gsh chunks), 4 (ue8m0 word)
+        lead = (uint32_t)lane & (SK == SK_ROW ? 31u : SK == SK_E8M0 ? 3u : ((1u << m[0].gsh) - 1u) & 31u);
         const int my_tiles = tile_first < ntiles ? (ntiles - tile_first + tile_step - 1) / tile_step : 0;
         total = my_tiles * nsteps;
         issued = 0;
@@ -854,7 +907,7 @@ struct RowStreamer {
                     if (ct_c * 32 + lane < nchunks) {
                         const uint32_t slot = ring + (uint32_t)(p * SLOT);
                         Chunk<FMT> c[NR];
-                        float sc[NR];
+                        uint32_t sw[NR];     // scale words, each read at this lane's own slot position
 #pragma unroll
                         for (int rr = 0; rr < NR; rr++) {
                             if constexpr (FMT == FMT_INT3_G64) {
@@ -863,7 +916,24 @@ struct RowStreamer {
                             } else {
                                 c[rr].w = lds16(slot + rr * 512);
                             }
-                            sc[rr] = lds_f32(slot + S_OFF + rr * 128 - lane * 12);
+                            sw[rr] = lds_u32(slot + S_OFF + rr * 128 - lane * 12);
+                        }
+                        if constexpr (SH) {
+                            // lanes sharing a scale take the word of the lane that
+                            // copied it; the lanes here are a prefix of the warp
+                            // holding every such lane
+                            const int rem = nchunks - ct_c * 32;
+                            const uint32_t act = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
+#pragma unroll
+                            for (int rr = 0; rr < NR; rr++) sw[rr] = __shfl_sync(act, sw[rr], lane - (int)lead);
+                        }
+                        float sc[NR];
+#pragma unroll
+                        for (int rr = 0; rr < NR; rr++) {
+                            if constexpr (SK == SK_E8M0)   // byte lane & 3 of the word
+                                sc[rr] = e8m0_to_f32(__byte_perm(sw[rr], 0u, 0x4440u + (uint32_t)(lane & 3)));
+                            else
+                                sc[rr] = __uint_as_float(sw[rr]);
                         }
                         uint32_t xq[S];
 #pragma unroll

@@ -5,6 +5,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "qg_device.cuh"
 #include "qg_internal.h"
 
@@ -18,8 +20,27 @@
 namespace qg {
 namespace QG_CAT(fmt_, QG_NAME) {
 
-constexpr int FMT = QG_FMT;
+constexpr int QF = QG_FMT;                 // the format of this translation unit
+constexpr int FMT = decode_of(QF);         // its code decoding
+constexpr int SK = scale_kind_of(QF);      // its scales: per row, f32 per group, ue8m0 per group
 constexpr int EPL = Traits<FMT>::EPL;
+
+// Ring kernels with shared scales (see RowStreamer): always for row scales and
+// ue8m0 words; for the grouped int4/int8 formats when a group spans several
+// chunks (gsh > 0), picked per launch.
+constexpr bool kShareAlways = SK != SK_F32;
+constexpr bool kShareMaybe = SK == SK_F32 && (QF == FMT_INT4_G || QF == FMT_INT8_G);
+
+template <class F>
+static cudaError_t with_share(int gsh, F&& f)
+{
+    if constexpr (kShareMaybe) {
+        if (gsh > 0) return f(std::true_type{});
+        return f(std::false_type{});
+    } else {
+        return f(std::integral_constant<bool, kShareAlways>{});
+    }
+}
 
 // Rows per warp tile: up to 4 chunk rows (NM matrices x R rows) so each x
 // quad read from shared memory serves several rows, and at most 8
@@ -71,9 +92,9 @@ inline Mat to_mat(const HostMat& h)
     m.sc = h.sc;
     m.O = h.O;
     m.I = h.I;
-    m.ngrp = FMT == FMT_INT8_ROW ? 1 : h.I / h.gs;
-    int sh = 0;
-    if (FMT == FMT_INT4_G) while ((32 << sh) < h.gs) sh++;
+    m.ngrp = SK == SK_ROW ? 1 : h.I / h.gs;
+    int sh = 0;                            // groups are whole chunks: chunk q is in group q >> sh
+    if (SK != SK_ROW) while ((EPL << sh) < h.gs) sh++;
     m.gsh = sh;
     return m;
 }
@@ -173,10 +194,10 @@ struct ExpertUpJob : RingLayout, TileSource<2> {
         const long long e = batches[b].x;
         out[0] = gate0;
         out[0].w += e * mat_bytes;
-        out[0].sc += e * mat_scales;
+        out[0].sc = sc_ptr<SK>(out[0].sc, e * mat_scales);
         out[1] = up0;
         out[1].w += e * mat_bytes;
-        out[1].sc += e * mat_scales;
+        out[1].sc = sc_ptr<SK>(out[1].sc, e * mat_scales);
     }
     __device__ const float* xrow(int b, int s) const { return x + (long long)pair_tok[batches[b].y + s] * D; }
     __device__ void store(int b, int s, long long row, float v) const
@@ -222,7 +243,7 @@ struct ExpertDownJob : RingLayout, TileSource<1> {
         const long long e = batches[b].x;
         out[0] = down0;
         out[0].w += e * mat_bytes;
-        out[0].sc += e * mat_scales;
+        out[0].sc = sc_ptr<SK>(out[0].sc, e * mat_scales);
     }
     __device__ const float* xrow(int b, int s) const { return h + (long long)(batches[b].y + s) * F; }
     __device__ void store(int b, int s, long long row, float v) const
@@ -277,7 +298,7 @@ struct Sink {
 
 // One segment: rows [l0, l1) of batch b, all warps of the CTA, with the
 // batch's s_act <= S activation rows; warp w takes the row tiles w, w + W, ...
-template <int NM, int S, class Job, int RF = 0>
+template <int NM, int S, class Job, int RF = 0, bool SH = false>
 __device__ __forceinline__ void segment(const Job& job, int b, long long l0, long long l1, int s_act, float* xs,
                                         int& staged)
 {
@@ -285,7 +306,7 @@ __device__ __forceinline__ void segment(const Job& job, int b, long long l0, lon
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Mat m[NM];
     job.mats(b, m);
-    RowStreamer<FMT, S, R, kRing, NM, Job::kLoopS> st;
+    RowStreamer<QF, S, R, kRing, NM, Job::kLoopS, SH> st;
     const int ntiles = (int)((l1 - l0 + R - 1) / R);
     st.begin(m, l0, l1, warp, ntiles, (int)(blockDim.x >> 5), lane,
              (uint32_t)(job.ring_off + warp * job.ring_stride));   // copies in flight during staging
@@ -314,7 +335,7 @@ __device__ __forceinline__ void segment(const Job& job, int b, long long l0, lon
 // activation rows the code is built for; a batch may use fewer.  RF > 0
 // forces RF rows per tile (single rows for matrices too short to give every
 // warp a tile of the default height).
-template <int NM, int S, class Job, int RF = 0>
+template <int NM, int S, class Job, int RF = 0, bool SH = false>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ Job job)
 {
     float* xs = reinterpret_cast<float*>(qg_smem4);
@@ -332,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         const long long base = (long long)b * rows_per;
         const long long l0 = r - base;
         const long long l1 = (r_end - base) < rows_per ? (r_end - base) : rows_per;
-        segment<NM, S, Job, RF>(job, b, l0, l1, job.batch_S(b), xs, staged);
+        segment<NM, S, Job, RF, SH>(job, b, l0, l1, job.batch_S(b), xs, staged);
         r = base + l1;
     }
 }
@@ -397,7 +418,7 @@ __global__ void k_dequant(const Mat m, float* __restrict__ out)
         const int q = (int)(t - o * nchunks);
         Chunk<FMT> c;
         float sc;
-        load_chunk<FMT>(m, o, q, c, sc);
+        load_chunk<QF>(m, o, q, c, sc);
         float v[EPL];
         decode_chunk<FMT>(c, v);
         float* dst = out + o * m.I + (long long)q * EPL;
@@ -445,15 +466,16 @@ static bool plan_tile(int NM, int R, int I, int gs, int xrows, TileLayout& L)
     constexpr int KS = 32 * EPL;
     L.nslices = (I + KS - 1) / KS;
     L.xstride = L.nslices * KS;
-    L.sbox = FMT == FMT_INT8_ROW ? 0 : (KS / gs) * 4;
-    if (FMT != FMT_INT8_ROW && (KS % gs != 0 || L.sbox < 16)) return false;
+    // scale bytes per row per slice: none for one scale per row (read from global per tile)
+    L.sbox = SK == SK_ROW ? 0 : (KS / gs) * (SK == SK_E8M0 ? 1 : 4);
+    if (SK != SK_ROW && (KS % gs != 0 || L.sbox < 16)) return false;
     L.tx_bytes = NM * R * (512 + (FMT == FMT_INT3_G64 ? 256 : 0) + L.sbox);
     int off = 0;
     for (int m = 0; m < 2; m++) L.code_off[m] = L.b_off[m] = L.s_off[m] = 0;
     for (int m = 0; m < NM; m++) { L.code_off[m] = off; off = align_up(off + R * 512, 128); }
     if (FMT == FMT_INT3_G64)
         for (int m = 0; m < NM; m++) { L.b_off[m] = off; off = align_up(off + R * 256, 128); }
-    if (FMT != FMT_INT8_ROW)
+    if (SK != SK_ROW)
         for (int m = 0; m < NM; m++) { L.s_off[m] = off; off = align_up(off + R * L.sbox, 128); }
     L.slot_bytes = off;
     L.ring_off = align_up(xrows * L.xstride * 4, 128);
@@ -478,7 +500,7 @@ static bool tile_sources(TileSource<NM>& src, const void* const (&w)[NM], const 
 {
     const long long rb = code_row_bytes(I);
     const long long rbB = I / 8;
-    const long long sb = (long long)(I / gs) * 4;
+    const long long sb = (long long)(I / gs) * (SK == SK_E8M0 ? 1 : 4);   // scale bytes per row
     const long long total = E * mat_bytes;
     if (E * O >= (1ll << 31) || total / rb >= (1ll << 31) || (FMT == FMT_INT3_G64 && total / rbB >= (1ll << 31)))
         return false;     // tensor rows and tile indices are 32-bit in the kernel
@@ -487,8 +509,9 @@ static bool tile_sources(TileSource<NM>& src, const void* const (&w)[NM], const 
         if (!encode_rows_map(&src.tm[3 * m], w[m], total / rb, rb, 512, R, false)) return false;
         if (FMT == FMT_INT3_G64 && !encode_rows_map(&src.tm[3 * m + 1], w[m], total / rbB, rbB, 256, R, false))
             return false;
-        if (FMT != FMT_INT8_ROW &&
-            !encode_rows_map(&src.tm[3 * m + 2], sc[m], E * O, sb, src.tile.sbox, R, true))
+        // ue8m0 scale rows are moved as 4-byte elements: only bytes count
+        if (SK != SK_ROW &&
+            !encode_rows_map(&src.tm[3 * m + 2], sc[m], E * O, sb, src.tile.sbox, R, SK == SK_F32))
             return false;
     }
     src.row_mul[0] = mat_bytes / rb;
@@ -516,7 +539,7 @@ static cudaError_t launch_dense(const DenseJob<NM>& job_in, int grid, size_t x_b
     DenseJob<NM> job = job_in;
     constexpr int R = tile_rows_per<S, NM>();
     const int I = job.m[0].I;
-    const int gs = FMT == FMT_INT8_ROW ? I : I / job.m[0].ngrp;
+    const int gs = SK == SK_ROW ? I : I / job.m[0].ngrp;
     const void* w[NM];
     const float* sc[NM];
     for (int k = 0; k < NM; k++) {
@@ -525,32 +548,40 @@ static cudaError_t launch_dense(const DenseJob<NM>& job_in, int grid, size_t x_b
     }
     const long long O = job.m[0].O;
     const long long mat_bytes = FMT == FMT_INT3_G64 ? O * (I / 4) + O * (I / 8) : O * code_row_bytes(I);
-    // Measured on GB300: with one activation row the int8/int4/MXFP4 rows are
-    // cheap to decode and the per-lane copy kernel is a little faster; int3
-    // and several activation rows go to the tile kernel.
+    // Measured on GB300: with one activation row and one scale per lane the
+    // int8/int4/MXFP4 rows are cheap to decode and the per-lane copy kernel is
+    // a little faster; int3, several activation rows, and -- on matrices with
+    // enough rows per CTA for full tiles -- scales shared by several lanes
+    // (rows, ue8m0 words, long groups) go to the tile kernel.
     const int policy = kernel_policy();
-    const bool prefer_tile = policy == QKERNEL_TILE || (policy == QKERNEL_AUTO && (S > 1 || FMT == FMT_INT3_G64));
+    const bool short_matrix = (O + grid - 1) / grid < (long long)kWarps * rows_per_tile<1, NM>();
+    const bool shares = (kShareAlways || (kShareMaybe && job.m[0].gsh > 0)) && !short_matrix;
+    const bool prefer_tile =
+        policy == QKERNEL_TILE || (policy == QKERNEL_AUTO && (S > 1 || FMT == FMT_INT3_G64 || shares));
     if (prefer_tile && plan_tile(NM, R, I, gs, S, job.tile) &&
         tile_sources<NM>(job, w, sc, 1, O, I, gs, mat_bytes, R))
         return launch_tile<NM, S>(job, grid, st);
-    if constexpr (S == 1) {
-        // fewer rows per CTA than warps x tile height: single-row tiles keep more warps busy
-        if ((O + grid - 1) / grid < (long long)kWarps * rows_per_tile<1, NM>()) {
-            auto kern1 = k_stream<NM, 1, DenseJob<NM>, 1>;
-            job.ring_stride = kRing * ring_slot_bytes<FMT, NM>();
-            const size_t smem1 = x_bytes + (size_t)kWarps * job.ring_stride;
-            static int granted1[64];
-            cudaError_t e = set_smem(kern1, smem1, granted1);
-            if (e != cudaSuccess) return e;
-            return launch_pdl(kern1, dim3(grid), dim3(kThreads), smem1, st, job);
+    return with_share(job.m[0].gsh, [&](auto sh) -> cudaError_t {
+        constexpr bool SH = decltype(sh)::value;
+        if constexpr (S == 1) {
+            // fewer rows per CTA than warps x tile height: single-row tiles keep more warps busy
+            if (short_matrix) {
+                auto kern1 = k_stream<NM, 1, DenseJob<NM>, 1, SH>;
+                job.ring_stride = kRing * ring_slot_bytes<FMT, NM>();
+                const size_t smem1 = x_bytes + (size_t)kWarps * job.ring_stride;
+                static int granted1[64];
+                cudaError_t e = set_smem(kern1, smem1, granted1);
+                if (e != cudaSuccess) return e;
+                return launch_pdl(kern1, dim3(grid), dim3(kThreads), smem1, st, job);
+            }
         }
-    }
-    auto kern = k_stream<NM, S, DenseJob<NM>>;
-    const size_t smem = x_bytes + (size_t)kWarps * job.ring_stride;
-    static int granted[64];
-    cudaError_t e = set_smem(kern, smem, granted);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
+        auto kern = k_stream<NM, S, DenseJob<NM>, 0, SH>;
+        const size_t smem = x_bytes + (size_t)kWarps * job.ring_stride;
+        static int granted[64];
+        cudaError_t e = set_smem(kern, smem, granted);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
+    });
 }
 
 template <int NM>
@@ -609,7 +640,7 @@ cudaError_t QG_CAT(gate_up_, QG_NAME)(const HostMat& g, const HostMat& u, const 
 cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st)
 {
     const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
-    const int gs = FMT == FMT_INT8_ROW ? a.D : a.gs;
+    const int gs = SK == SK_ROW ? a.D : a.gs;
     ExpertUpJob job;
     job.gate0 = to_mat(HostMat{a.gate, a.gate_s, a.F, a.D, gs});
     job.up0 = to_mat(HostMat{a.up, a.up_s, a.F, a.D, gs});
@@ -639,18 +670,20 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
             tile_sources<2>(job, w, sc, a.E, a.F, a.D, gs, job.mat_bytes, R))
             return launch_tile<2, kExpertSmax>(job, grid, st);
     }
-    auto kern = k_stream<2, kExpertSmax, ExpertUpJob>;
-    const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
-    static int granted[64];
-    cudaError_t e = set_smem(kern, smem, granted);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
+    return with_share(job.gate0.gsh, [&](auto sh) -> cudaError_t {
+        auto kern = k_stream<2, kExpertSmax, ExpertUpJob, 0, decltype(sh)::value>;
+        const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
+        static int granted[64];
+        cudaError_t e = set_smem(kern, smem, granted);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
+    });
 }
 
 cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st)
 {
     const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
-    const int gs = FMT == FMT_INT8_ROW ? a.F : a.gs;
+    const int gs = SK == SK_ROW ? a.F : a.gs;
     ExpertDownJob job;
     job.down0 = to_mat(HostMat{a.down, a.down_s, a.D, a.F, gs});
     job.mat_bytes = FMT == FMT_INT8_ROW ? (long long)a.D * a.F
@@ -676,12 +709,14 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
             tile_sources<1>(job, w, sc, a.E, a.D, a.F, gs, job.mat_bytes, R))
             return launch_tile<1, kExpertSmax>(job, grid, st);
     }
-    auto kern = k_stream<1, kExpertSmax, ExpertDownJob>;
-    const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
-    static int granted[64];
-    cudaError_t e = set_smem(kern, smem, granted);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
+    return with_share(job.down0.gsh, [&](auto sh) -> cudaError_t {
+        auto kern = k_stream<1, kExpertSmax, ExpertDownJob, 0, decltype(sh)::value>;
+        const size_t smem = job.ring_off + (size_t)kWarps * job.ring_stride;
+        static int granted[64];
+        cudaError_t e = set_smem(kern, smem, granted);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
+    });
 }
 
 int QG_CAT(device_error_, QG_NAME)(int clear)

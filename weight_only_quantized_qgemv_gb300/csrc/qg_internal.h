@@ -126,9 +126,12 @@ bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long lo
     int device_error_##name(int clear);
 
 QG_DECLARE_FMT(int8)
+QG_DECLARE_FMT(int8g)
+QG_DECLARE_FMT(int4r)
 QG_DECLARE_FMT(int4)
 QG_DECLARE_FMT(int3)
 QG_DECLARE_FMT(mxfp4)
+QG_DECLARE_FMT(mxfp4e)
 
 #undef QG_DECLARE_FMT
 

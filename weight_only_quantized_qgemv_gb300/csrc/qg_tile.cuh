@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
                 if constexpr (FMT == FMT_INT3_G64)
                     tma_load_2d(dst + B_OFF + m * R * PLANE_B_ROW, &job.tm[3 * m + 1], pk * (PLANE_B_ROW / 4), prow1,
                                 bar);
-                if constexpr (FMT != FMT_INT8_ROW)
+                if constexpr (SK != SK_ROW)
                     tma_load_2d(dst + s_off0 + m * s_step, &job.tm[3 * m + 2], pk * (sbox / 4), prow2, bar);
             }
         }
@@ -191,8 +191,9 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
         const long long rows = job.rows_per();
         // this lane's scale offsets inside a slot, per chunk row
         [[maybe_unused]] uint32_t sso[NR];
-        if constexpr (FMT != FMT_INT8_ROW) {
-            const uint32_t ls = s_off0 + (((uint32_t)lane >> mt[0].gsh) << 2);
+        if constexpr (SK != SK_ROW) {
+            // f32: 4 bytes per group; ue8m0: one byte per group (one group per lane)
+            const uint32_t ls = s_off0 + (((uint32_t)lane >> mt[0].gsh) << (SK == SK_E8M0 ? 0 : 2));
 #pragma unroll
             for (int m = 0; m < NM; m++)
 #pragma unroll
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
 #pragma unroll
                 for (int rr = 0; rr < NR; rr++) acc[s][rr] = 0.f;
             [[maybe_unused]] float rsc[NR];
-            if constexpr (FMT == FMT_INT8_ROW) {
+            if constexpr (SK == SK_ROW) {
 #pragma unroll
                 for (int m = 0; m < NM; m++)
 #pragma unroll
@@ -232,7 +233,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
                         } else {
                             ch[rr].w = lds16(sl + (m * R + r) * CODE_ROW);
                         }
-                        if constexpr (FMT == FMT_INT8_ROW) sc[rr] = rsc[rr];
+                        if constexpr (SK == SK_ROW) sc[rr] = rsc[rr];
+                        else if constexpr (SK == SK_E8M0) sc[rr] = e8m0_to_f32(lds_u8(so + sso[rr]));
                         else sc[rr] = lds_f32(so + sso[rr]);
                     }
                 uint32_t xq[S];

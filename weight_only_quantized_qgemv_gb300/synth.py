@@ -14,6 +14,9 @@ Layouts drawn (the library's ABI):
   int3-g64       plane A [O][I/4] then plane B [O][I/8] in one buffer,
                  f32 scales [O][I/64]
   MXFP4          [O][I/2] bytes of e2m1 nibbles, f32 scales [O][I/32]
+  int4 per row   the int4 layout, one f32 scale per row
+  int8 grouped   the int8 layout, f32 scales [O][I/gs]
+  MXFP4 ue8m0    the MXFP4 layout, uint8 scale exponent bytes [O][I/32]
 """
 from __future__ import annotations
 
@@ -21,35 +24,44 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-# Format ids as colibri numbers its quantized storages (fmt 1, 4, 5, 7).
+# Format ids as colibri numbers its quantized storages (fmt 1, 2, 4, 5, 7, 8, 13).
 INT8_ROW = 1
+INT4_ROW = 2
 INT4_G = 4
 INT3_G64 = 5
 MXFP4_G32 = 7
+MXFP4_E8M0 = 8
+INT8_G = 13
 
-FMT_NAMES = {INT8_ROW: "int8_row", INT4_G: "int4_g", INT3_G64: "int3_g64", MXFP4_G32: "mxfp4_g32"}
+FMT_NAMES = {INT8_ROW: "int8_row", INT4_ROW: "int4_row", INT4_G: "int4_g", INT3_G64: "int3_g64",
+             MXFP4_G32: "mxfp4_g32", MXFP4_E8M0: "mxfp4_e8m0", INT8_G: "int8_g"}
 
 
 def fixed_group(fmt: int, I: int, gs: int | None = None) -> int:
     """Group size implied by a format (int8 per row: the whole row)."""
-    if fmt == INT8_ROW:
+    if fmt in (INT8_ROW, INT4_ROW):
         return I
     if fmt == INT3_G64:
         return 64
-    if fmt == MXFP4_G32:
+    if fmt in (MXFP4_G32, MXFP4_E8M0):
         return 32
     return 32 if gs is None else gs
 
 
 def packed_bytes(fmt: int, O: int, I: int) -> int:
     """Bytes of one packed [O][I] matrix."""
-    if fmt == INT8_ROW:
+    if fmt in (INT8_ROW, INT8_G):
         return O * I
-    if fmt in (INT4_G, MXFP4_G32):
+    if fmt in (INT4_ROW, INT4_G, MXFP4_G32, MXFP4_E8M0):
         return O * I // 2
     if fmt == INT3_G64:
         return O * I // 4 + O * I // 8
     raise ValueError(f"unknown fmt {fmt}")
+
+
+def scale_itemsize(fmt: int) -> int:
+    """Bytes of one stored scale: one ue8m0 byte, else an f32."""
+    return 1 if fmt == MXFP4_E8M0 else 4
 
 
 def generator(seed: int, *spawn_key: int) -> np.random.Generator:
@@ -63,7 +75,7 @@ def draw_packed(fmt: int, O: int, I: int, rng: np.random.Generator) -> np.ndarra
     Uniform codes in every nibble, pair or bit are uniform bytes, which come
     straight from the generator's raw 64-bit output.
     """
-    if fmt == INT8_ROW:
+    if fmt in (INT8_ROW, INT8_G):
         return rng.integers(-127, 128, size=O * I, dtype=np.int8).view(np.uint8)
     n = packed_bytes(fmt, O, I)
     raw = rng.bit_generator.random_raw((n + 7) // 8).view(np.uint8)
@@ -71,9 +83,22 @@ def draw_packed(fmt: int, O: int, I: int, rng: np.random.Generator) -> np.ndarra
 
 
 def draw_scales(O: int, I: int, gs: int, rng: np.random.Generator, kind: str,
-                mu: float = -4.0, sigma: float = 0.5) -> np.ndarray:
-    """f32 scales [O][I/gs]: 'lognormal' (mu, sigma) or 'pow2' (2^k, k uniform in [-8, 0])."""
+                mu: float = -4.0, sigma: float = 0.5, fmt: int | None = None) -> np.ndarray:
+    """f32 scales [O][I/gs]: 'lognormal' (mu, sigma) or 'pow2' (2^k, k uniform in [-8, 0]).
+
+    fmt=MXFP4_E8M0 draws the stored exponent bytes 127 + k instead: k uniform
+    in [-8, 0] ('pow2'), or k = round(log2 of a lognormal(mu, sigma) draw).
+    """
     n = O * (I // gs)
+    if fmt == MXFP4_E8M0:
+        if kind == "pow2":
+            k = rng.integers(-8, 1, size=n)
+        elif kind == "lognormal":
+            z = rng.standard_normal(size=n)
+            k = np.rint((z * sigma + mu) / np.log(2.0)).astype(np.int64)
+        else:
+            raise ValueError(kind)
+        return (127 + k).astype(np.uint8)
     if kind == "lognormal":
         z = rng.standard_normal(size=n, dtype=np.float32)
         return np.exp(z * np.float32(sigma) + np.float32(mu)).astype(np.float32)
@@ -123,13 +148,13 @@ class GemvWorkload:
 
     @property
     def scale_bytes(self) -> int:
-        return 4 * self.O * (self.I // self.gs)
+        return scale_itemsize(self.fmt) * self.O * (self.I // self.gs)
 
     def weights(self, copy: int = 0):
-        """(packed uint8, scales f32) for weight copy `copy` (copies differ, same law)."""
+        """(packed uint8, scales f32 or ue8m0 bytes) for weight copy `copy` (copies differ, same law)."""
         rng = generator(self.seed, 1, copy)
         w = draw_packed(self.fmt, self.O, self.I, rng)
-        sc = draw_scales(self.O, self.I, self.gs, rng, self.scale_kind, self.scale_mu)
+        sc = draw_scales(self.O, self.I, self.gs, rng, self.scale_kind, self.scale_mu, fmt=self.fmt)
         return w, sc
 
     def x(self):
@@ -162,7 +187,7 @@ class ExpertWorkload:
         tot = 0
         for which in (self.GATE, self.UP, self.DOWN):
             O, I = self.matrix_shape(which)
-            tot += packed_bytes(self.fmt, O, I) + 4 * O * (I // self.gs)
+            tot += packed_bytes(self.fmt, O, I) + scale_itemsize(self.fmt) * O * (I // self.gs)
         return tot
 
     def expert_matrix(self, e: int, which: int):
@@ -170,7 +195,7 @@ class ExpertWorkload:
         O, I = self.matrix_shape(which)
         rng = generator(self.seed, 10, e, which)
         w = draw_packed(self.fmt, O, I, rng)
-        sc = draw_scales(O, I, self.gs, rng, self.scale_kind, self.scale_mu)
+        sc = draw_scales(O, I, self.gs, rng, self.scale_kind, self.scale_mu, fmt=self.fmt)
         return w, sc
 
     MATRICES = (("gate", 0), ("up", 1), ("down", 2))
@@ -203,7 +228,7 @@ class ExpertWorkload:
         for name, which in self.MATRICES:
             nb, ns = self.sizes(which)
             out[name] = np.empty(len(experts) * nb, dtype=np.uint8)
-            out[name + "_s"] = np.empty(len(experts) * ns, dtype=np.float32)
+            out[name + "_s"] = np.empty(len(experts) * ns, dtype=np.uint8 if self.fmt == MXFP4_E8M0 else np.float32)
 
         def sink(name, slot, w, sc):
             nb, ns = w.size, sc.size
@@ -242,6 +267,17 @@ def workload(name: str):
         "int4_g32_experts_E256_D6144_F2048_s8_k8": ExpertWorkload("int4_g32_experts_E256_D6144_F2048_s8_k8",
                                                                   INT4_G, 256, 6144, 2048, 8, 8, 32,
                                                                   "lognormal", -4.0, 1005),
+        # Storage variants of the same decoders: int4 with one scale per row,
+        # int8 with one scale per 64 inputs, and the MXFP4 expert workload with
+        # its scales as ue8m0 exponent bytes (same seed and exponent draws as
+        # the f32 one above, so the two hold the same values).
+        "int4_row_16384x6144_s1": GemvWorkload("int4_row_16384x6144_s1", INT4_ROW, 16384, 6144, 1, 6144,
+                                                "lognormal", -6.0, 1006),
+        "int8_g64_16384x6144_s1": GemvWorkload("int8_g64_16384x6144_s1", INT8_G, 16384, 6144, 1, 64,
+                                                "lognormal", -7.0, 1007),
+        "mxfp4_e8m0_experts_E256_D6144_F2048_s1_k8": ExpertWorkload("mxfp4_e8m0_experts_E256_D6144_F2048_s1_k8",
+                                                                    MXFP4_E8M0, 256, 6144, 2048, 1, 8, 32,
+                                                                    "pow2", 0.0, 1004),
     }
     return table[name]
 
@@ -253,4 +289,12 @@ WORKLOADS = [
     "int3_g64_6144x16384_s1",
     "mxfp4_experts_E256_D6144_F2048_s1_k8",
     "int4_g32_experts_E256_D6144_F2048_s8_k8",
+]
+
+# Workloads of the storage variants (measured like the ones above, not part of
+# the default set).
+VARIANT_WORKLOADS = [
+    "int4_row_16384x6144_s1",
+    "int8_g64_16384x6144_s1",
+    "mxfp4_e8m0_experts_E256_D6144_F2048_s1_k8",
 ]
