@@ -221,6 +221,28 @@ int qexpert_group_noalloc(int fmt, int gs,
 int qdequant(int fmt, int gs, const void* w, const float* scales,
              int O, int I, float* out, void* stream);
 
+/*
+ * The prefill GEMM: y[t][o] = sum_i value(W[o][i]) * scales[o][i/gs] * x[t][i]
+ * for many activation rows t < s, on the tensor cores -- the tiled GEMM that
+ * colibri's docs/vulkan.md (the tiled-GEMM and cooperative-matrix paragraph)
+ * takes instead of the per-row GEMV from two rows on.  Weight codes are
+ * decoded exactly to f16; every activation row is scaled by a power of two
+ * and split into two f16 parts (22 significand bits; written to the
+ * workspace), the MMA runs on both, and each group of gs inputs (at most 128
+ * at a time) sums into a fresh f32 partial that is added to the row's sum
+ * times the group scale.  The result meets the f32 GEMV's error bound, not
+ * its bits.
+ *   w, scales, x, y as for qgemv;  workspace of ws_bytes >= qgemm_workspace(I,
+ *   s) device bytes, 256-byte aligned, contents on entry irrelevant.
+ * Every format, with I % 64 == 0 and groups of at least 32 inputs
+ * (QFMT_INT8_G with gs 16: QSTATUS_BAD_FMT).  Intended for s >= 16; any s >= 1
+ * works.  I <= 2^20, s <= 65536.
+ */
+size_t qgemm_workspace(int I, int s);
+int qgemm(int fmt, int gs, const void* w, const float* scales,
+          const float* x, int O, int I, int s, float* y,
+          void* workspace, size_t ws_bytes, void* stream);
+
 /* A static description of a status code. */
 const char* qstatus_string(int status);
 

@@ -136,3 +136,23 @@ def test_kernel_policy_round_trip(L):
         assert _lib.qkernel_policy(_lib.QKERNEL_AUTO) == _lib.QKERNEL_RING
     finally:
         _lib.qkernel_policy(prev)
+
+
+def test_qgemm_checks(L):
+    """The prefill GEMM's host-side checks (nothing is enqueued)."""
+    Z = ctypes.c_size_t
+    L.qgemm.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + \
+        [ctypes.c_void_p, ctypes.c_void_p, Z, ctypes.c_void_p]
+    L.qgemm_workspace.argtypes = [ctypes.c_int, ctypes.c_int]
+    L.qgemm_workspace.restype = Z
+    ws = L.qgemm_workspace(6144, 512)
+    assert ws >= 2 * 512 * 6144 * 2 + 512 * 4
+    assert L.qgemm_workspace(6144, 20) == L.qgemm_workspace(6144, 32)     # rows padded to a 32-row tile
+    assert L.qgemm_workspace(0, 4) == 0
+    assert L.qgemm(4, 32, A, A, A, 16, 6176, 512, A, A, ws, None) == -2     # I not a multiple of 64
+    assert L.qgemm(13, 16, A, A, A, 16, 1024, 64, A, A, ws, None) == -1     # partials need 32 inputs
+    assert L.qgemm(3, 0, A, A, A, 16, 1024, 64, A, A, ws, None) == -1       # unknown format
+    assert L.qgemm(4, 32, A, A, A, 16, 6144, 512, A, A, ws - 1, None) == -5  # workspace too small
+    assert L.qgemm(4, 32, A, A, A, 16, 6144, 512, A, None, ws, None) == -4   # no workspace
+    assert L.qgemm(4, 32, A, A, A, 16, 6144, 512, A, A + 16, ws, None) == -3  # workspace not 256-aligned
+    assert L.qgemm(4, 32, A, A, A, 16, 6144, 0, A, A, ws, None) == -2       # s < 1

@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
         L.qgate_up_act.restype = I
         L.qexpert_group_act.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, P, P, I, Fl, P, P, Z, P, P]
         L.qexpert_group_act.restype = I
+        L.qgemm_workspace.argtypes = [I, I]
+        L.qgemm_workspace.restype = Z
+        L.qgemm.argtypes = [I, I, P, P, P, I, I, I, P, P, Z, P]
+        L.qgemm.restype = I
         L.qdequant.argtypes = [I, I, P, P, I, I, P, P]
         L.qdequant.restype = I
         L.qstatus_string.argtypes = [I]
@@ -160,6 +164,15 @@ def qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x,
                                    _ptr(down_s), E, D, F, _ptr(x), s, k, _ptr(ids), _ptr(wts), int(act),
                                    float(limit), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status_dev),
                                    _stream(stream)))
+
+
+def qgemm_workspace(I, s) -> int:
+    return int(lib().qgemm_workspace(I, s))
+
+
+def qgemm(fmt, gs, w, scales, x, O, I, s, y, workspace, ws_bytes, stream=None):
+    _check(lib().qgemm(fmt, gs, _ptr(w), _ptr(scales), _ptr(x), O, I, s, _ptr(y), _ptr(workspace), int(ws_bytes),
+                       _stream(stream)))
 
 
 def qdequant(fmt, gs, w, scales, O, I, out, stream=None):

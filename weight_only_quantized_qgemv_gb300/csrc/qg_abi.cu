@@ -84,6 +84,8 @@ static int check_fmt(int fmt, int gs, int I, int* gs_out)
 }
 
 constexpr int kMaxI = 51200;   // an upper bound; the shared-memory budget below decides
+constexpr int kGemmMaxI = 1 << 20;   // qgemm: tensor-map and index ranges
+constexpr int kGemmMaxS = 1 << 16;
 
 // Shared memory left for activation rows once the copy rings of a launch of
 // format fmt with nm matrices per row tile are placed.
@@ -293,6 +295,20 @@ bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long lo
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_x_map(CUtensorMap* map, const void* base, long long rows, long long cols, int box_rows)
+{
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || rows < box_rows || cols <= 0 || cols % 64 || box_rows < 1 || box_rows > 256 || !aligned(base, 16))
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace qg
 
 using namespace qg;
@@ -486,6 +502,46 @@ int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, co
     e = expert_combine(a, cs);
     if (e != cudaSuccess) return launch_status(e);
     return QSTATUS_OK;
+}
+
+size_t qgemm_workspace(int I, int s)
+{
+    if (I < 1 || s < 1) return 0;
+    return gemm_ws_layout(I, s).total;
+}
+
+int qgemm(int fmt, int gs, const void* w, const float* scales, const float* x, int O, int I, int s, float* y,
+          void* workspace, size_t ws_bytes, void* stream)
+{
+    int g = 0;
+    int st = check_fmt(fmt, gs, I, &g);
+    if (st) return st;
+    if (g < 32) return QSTATUS_BAD_FMT;                     // partials of at least 32 inputs
+    if (O < 1 || I < 1 || s < 1 || I % 64 || I > kGemmMaxI || s > kGemmMaxS) return QSTATUS_BAD_DIM;
+    if (!w || !scales || !x || !y || !workspace) return QSTATUS_NULL;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(scales, 4) || !aligned(y, 4) || !aligned(workspace, 256))
+        return QSTATUS_MISALIGNED;
+    const GemmWs L = gemm_ws_layout(I, s);
+    if (ws_bytes < L.total) return QSTATUS_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    GemmArgs a;
+    a.xh = ws + L.xh;
+    a.xl = ws + L.xl;
+    a.pexp = reinterpret_cast<const int32_t*>(ws + L.pexp);
+    a.s = s;
+    a.sp = gemm_rows(s);
+    a.y = y;
+    // the decoders' input order: int4 nibble pairs (q, q + 4), int3 (q, q + 8)
+    const int perm = (fmt == QFMT_INT4_G || fmt == QFMT_INT4_ROW) ? 8 : (fmt == QFMT_INT3_G64 ? 16 : 0);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = gemm_split_x(x, s, a.sp, I, perm, ws + L.xh, ws + L.xl, reinterpret_cast<int32_t*>(ws + L.pexp),
+                                 cs);
+    if (e != cudaSuccess) return launch_status(e);
+    const HostMat m{w, scales, O, I, g};
+#define QG_CALL(name) gemm_##name(m, a, cs)
+    QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+    return launch_status(e);
 }
 
 int qdequant(int fmt, int gs, const void* w, const float* scales, int O, int I, float* out, void* stream)

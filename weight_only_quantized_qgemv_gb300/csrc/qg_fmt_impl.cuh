@@ -600,6 +600,8 @@ static cudaError_t launch_dense_s(const DenseJob<NM>& job, int s, int grid, size
     }
 }
 
+#include "qg_gemm.cuh"
+
 }  // namespace fmt_<name>
 
 using namespace QG_CAT(fmt_, QG_NAME);
@@ -738,6 +740,15 @@ int QG_CAT(tile_rows_, QG_NAME)(int nm)
 size_t QG_CAT(ring_bytes_, QG_NAME)(int nm)
 {
     return (size_t)kWarps * (nm == 2 ? ring_stride_bytes<2>() : ring_stride_bytes<1>());
+}
+
+cudaError_t QG_CAT(gemm_, QG_NAME)(const HostMat& hm, const GemmArgs& g, cudaStream_t st)
+{
+    switch (gemm_bn(g.s)) {
+    case 32: return launch_gemm<32>(hm, g, st);
+    case 64: return launch_gemm<64>(hm, g, st);
+    default: return launch_gemm<128>(hm, g, st);
+    }
 }
 
 cudaError_t QG_CAT(dequant_, QG_NAME)(const HostMat& hm, float* out, cudaStream_t st)

@@ -111,6 +111,47 @@ struct TileLayout {
 bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long long row_bytes, int box_bytes,
                      int box_rows, bool f32);
 
+// The prefill GEMM's activations (workspace of qgemm): x rows scaled by 2^pexp
+// and split into f16 high and low parts, rows padded with zeros to a whole
+// number of activation-row tiles.
+struct GemmArgs {
+    const void* xh;           // f16 [sp][I]
+    const void* xl;           // f16 [sp][I]
+    const int32_t* pexp;      // [sp]
+    int s;                    // activation rows (y has s rows)
+    int sp;                   // padded rows
+    float* y;                 // [s][O]
+};
+
+// Activation rows per tile of the prefill GEMM for s rows, and the padded row
+// count of its workspace.
+inline int gemm_bn(int s) { return s <= 32 ? 32 : (s <= 64 ? 64 : 128); }
+inline int gemm_rows(int s) { const int bn = gemm_bn(s); return (s + bn - 1) / bn * bn; }
+
+struct GemmWs {
+    size_t xh, xl, pexp, total;
+};
+inline GemmWs gemm_ws_layout(int I, int s)
+{
+    const size_t sp = (size_t)gemm_rows(s);
+    GemmWs L;
+    size_t off = 0;
+    L.xh = off;   off = align256(off + sp * (size_t)I * 2);
+    L.xl = off;   off = align256(off + sp * (size_t)I * 2);
+    L.pexp = off; off = align256(off + sp * sizeof(int32_t));
+    L.total = off;
+    return L;
+}
+
+// Tensor map over an f16 [rows][cols] matrix (cols a multiple of 64) read in
+// boxes of 64 columns x box_rows rows with the 128-byte swizzle.
+bool encode_x_map(CUtensorMap* map, const void* base, long long rows, long long cols, int box_rows);
+
+// Writes the prefill GEMM's activation parts (qg_gemm_x.cu); perm is the
+// weight decoder's input order inside blocks of perm inputs (0: in order).
+cudaError_t gemm_split_x(const float* x, int s, int sp, int I, int perm, void* xh, void* xl, int32_t* pexp,
+                         cudaStream_t st);
+
 // Per-format launchers (defined in qg_fmt_<format>.cu).  Each returns a
 // cudaError_t of the launch.
 #define QG_DECLARE_FMT(name)                                                                            \
@@ -121,6 +162,7 @@ bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, long lo
     cudaError_t expert_up_##name(const ExpertArgs& a, int grid, cudaStream_t st);                       \
     cudaError_t expert_down_##name(const ExpertArgs& a, int grid, cudaStream_t st);                     \
     cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);                         \
+    cudaError_t gemm_##name(const HostMat& m, const GemmArgs& g, cudaStream_t st);                     \
     size_t ring_bytes_##name(int nm);                                                                 \
     int tile_rows_##name(int nm);                                                                     \
     int device_error_##name(int clear);
