@@ -40,6 +40,7 @@ from weight_only_quantized_qgemv_gb300 import synth  # noqa: E402
 METRIC = "achieved weight-stream GB/s (% of GB300 HBM peak); µs per fused expert group"
 DEFAULT_WORKLOAD = "int4_g32_16384x6144_s1"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TENSOR_TFLOPS = 1900.0
 NOMINAL_HBM_GBS = 8000.0
 FMT_LABEL = {1: "int8-row", 2: "int4-row", 4: "int4-g", 5: "int3-g64", 7: "mxfp4-g32", 8: "mxfp4-e8m0-g32",
              13: "int8-g"}
@@ -94,6 +95,18 @@ def hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense f16 tensor peak for the prefill GEMM: the measured bf16 burst figure
+    (f16 and bf16 run at the same nominal dense rate), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "bf16_tflops of measured (f16 = bf16 dense rate)"
+    except Exception:
+        return FALLBACK_TENSOR_TFLOPS, "fallback 1.9 PFLOP/s bf16 (f16 = bf16 dense rate)"
 
 
 class ClockSampler:
@@ -195,13 +208,24 @@ class GemvBench:
         self.y = torch.empty(wl.s, wl.O, dtype=torch.float32, device=device)
         self.gs = wl.gs if wl.fmt in GROUPED else 0
         self.launches_per_step = 1
+        if wl.gemm:     # prefill: the tensor-core GEMM, its x split and its workspace
+            from weight_only_quantized_qgemv_gb300 import qgemm_workspace
+            self.ws_bytes = qgemm_workspace(wl.I, wl.s)
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+            self.launches_per_step = 2
         self.l2_note = f"rotates {self.ncopies} weight copies ({self.ncopies * self.step_bytes / 1e6:.0f} MB > 2x L2)"
 
-    def step(self, i, stream):
-        from weight_only_quantized_qgemv_gb300 import qgemv
-        c = i % self.ncopies
+    def call(self, c, stream):
+        from weight_only_quantized_qgemv_gb300 import qgemm, qgemv
         wl = self.wl
-        qgemv(wl.fmt, self.gs, self.w[c], self.sc[c], self.x, wl.O, wl.I, wl.s, self.y, stream)
+        if wl.gemm:
+            qgemm(wl.fmt, self.gs, self.w[c], self.sc[c], self.x, wl.O, wl.I, wl.s, self.y, self.ws, self.ws_bytes,
+                  stream)
+        else:
+            qgemv(wl.fmt, self.gs, self.w[c], self.sc[c], self.x, wl.O, wl.I, wl.s, self.y, stream)
+
+    def step(self, i, stream):
+        self.call(i % self.ncopies, stream)
 
     def bytes_of(self, i):
         return self.step_bytes
@@ -213,11 +237,8 @@ class GemvBench:
         return self.x_pin.numel() * 4, self.y_pin.numel() * 4
 
     def e2e_step(self, i, stream):
-        from weight_only_quantized_qgemv_gb300 import qgemv
-        wl = self.wl
-        c = i % self.ncopies
         self.x.copy_(self.x_pin, non_blocking=True)
-        qgemv(wl.fmt, self.gs, self.w[c], self.sc[c], self.x, wl.O, wl.I, wl.s, self.y, stream)
+        self.call(i % self.ncopies, stream)
         self.y_pin.copy_(self.y, non_blocking=True)
 
     def config(self):
@@ -406,7 +427,10 @@ def gemv_kernel_name(wl, sms=152):
     """The kernel one qgemv call of this workload runs (the library's automatic choice):
     the tile kernel for int3 and several activation rows, and for one row when
     lanes share scales (per-row scales, ue8m0 words, groups longer than a
-    chunk) on a matrix with at least 64 rows per SM and a tile plan that fits."""
+    chunk) on a matrix with at least 64 rows per SM and a tile plan that fits.
+    Prefill workloads run qgemm."""
+    if wl.gemm:
+        return "whole qgemm call (k_gemm_split_x + k_gemm, tcgen05)"
     if wl.s > 1 or wl.fmt == synth.INT3_G64:
         return "k_tile"
     int8 = wl.fmt in (synth.INT8_ROW, synth.INT8_G)
@@ -442,7 +466,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOADS + synth.VARIANT_WORKLOADS)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=synth.WORKLOADS + synth.VARIANT_WORKLOADS + synth.PREFILL_WORKLOADS)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph-len", type=int, default=64, help="calls captured per CUDA graph replay")
@@ -455,7 +480,9 @@ def main():
     world, rank, local = dist_env()
     if args.steps is None:
         # about one second of timed device work, so the clock samples mean something
-        if isinstance(wl, synth.GemvWorkload):
+        if isinstance(wl, synth.GemvWorkload) and wl.gemm:
+            est = 2.0 * wl.O * wl.I * wl.s / 2e14 + 30e-6
+        elif isinstance(wl, synth.GemvWorkload):
             est = (wl.weight_bytes + wl.scale_bytes) / 6e12 + 3e-6
         else:
             est = 0.9 * wl.s * wl.k * wl.expert_bytes() / 6e12 + 12e-6
@@ -555,18 +582,29 @@ def main():
         cpu = cpu_baseline(wl, args.sample_seconds or 12.0, args.swiglu_limit)
     cfg = bench.config()
     cfg["graph_calls_per_replay"] = G
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_src}",
+            "frac_of_8000": achieved / NOMINAL_HBM_GBS,
+            "traffic": recorded_traffic(wl.name),
+            "algorithmic_bytes_per_launch": nbytes / steps_done,
+            "kernel": gemv_kernel_name(wl) if isinstance(bench, GemvBench)
+            else "whole qexpert_group call (prep + gate/up + down + combine)"}
+    if isinstance(wl, synth.GemvWorkload) and wl.gemm:
+        # a prefill batch is a dense contraction: the tensor roofline, on the
+        # algorithmic 2 O I s flops (the two-part split of x doubles the MMAs)
+        tpeak, tsrc = tensor_peak()
+        flops = 2.0 * wl.O * wl.I * wl.s
+        roof = {"bound": "tensor", "achieved": flops / per_launch_s / 1e12, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": flops / per_launch_s / 1e12 / tpeak, "peak_source": tsrc,
+                "traffic": recorded_traffic(wl.name), "algorithmic_flops_per_launch": flops,
+                "mma_flops_per_launch": 2 * flops, "weight_stream_gbs": achieved,
+                "kernel": gemv_kernel_name(wl)}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps_done,
         "warmup": args.warmup, "ms_per_step": t_max / steps_done * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "us_per_call": per_launch_s * 1e6,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_src}",
-                     "frac_of_8000": achieved / NOMINAL_HBM_GBS,
-                     "traffic": recorded_traffic(wl.name),
-                     "algorithmic_bytes_per_launch": nbytes / steps_done,
-                     "kernel": gemv_kernel_name(wl) if isinstance(bench, GemvBench)
-                     else "whole qexpert_group call (prep + gate/up + down + combine)"},
+        "roofline": roof,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": k_e2e, "us_per_step": t_e2e / k_e2e * 1e6},

@@ -28,8 +28,9 @@ namespace gemm {
 
 constexpr int kBM = 128;       // weight rows per tile (tensor-memory lanes)
 constexpr int kBK = 64;        // inputs per K step (one 128-byte row of f16)
-constexpr int kRowWarps = 4;   // warps with one thread per weight row
-constexpr int kThreads = 32 * kRowWarps + 32;   // + one warp issuing tensor copies and MMAs
+constexpr int kFoldWarps = 8;     // fold partials: warp w reads tensor-memory lanes 32 (w % 4).., columns half w / 4
+constexpr int kDecodeWarps = 4;   // decode the weights: one thread per weight row
+constexpr int kThreads = 32 * (kFoldWarps + kDecodeWarps + 1);   // + one warp issuing tensor copies and MMAs
 // 16-byte raw cells per row per K step: int8 64 B; int4 / e2m1 32 B; int3
 // 16 B of plane A and 8 B of plane B.
 constexpr int kCells = FMT == FMT_INT8_ROW ? 4 : 2;
@@ -43,14 +44,15 @@ template <int BN>
 struct Layout {
     static constexpr uint32_t kBBytes = 2 * BN * 128;     // x high part, then low part
     static constexpr int kBStages = BN == 128 ? 4 : 6;
-    static constexpr uint32_t kFixed = 2 * kABytes + kBStages * kBBytes + 8 * (kBStages + 4) + 16 + 1024;
+    static constexpr uint32_t kFixed = 2 * kABytes + kBStages * kBBytes + 4 * kBM * 8 + 8 * (kBStages + 10) + 16 + 1024;
     static constexpr int kRawStages = kFixed + 8 * (kRawBytes + kBM * 8) <= 225 * 1024 ? 8 : 6;
     static constexpr uint32_t kA = 0;
     static constexpr uint32_t kB = kA + 2 * kABytes;
     static constexpr uint32_t kRaw = kB + kBStages * kBBytes;
     static constexpr uint32_t kScl = kRaw + kRawStages * kRawBytes;   // per step and row: 8 bytes of scales
-    static constexpr uint32_t kBar = kScl + kRawStages * kBM * 8;      // kBStages + 2 + 2 barriers
-    static constexpr uint32_t kTmemSlot = kBar + 8 * (kBStages + 4);   // tensor-memory address, abort flag
+    static constexpr uint32_t kPScale = kScl + kRawStages * kBM * 8;   // 4 steps x rows: the folding scales
+    static constexpr uint32_t kBar = kPScale + 4 * kBM * 8;             // kBStages + 2 + 2 + 4 + 2 barriers
+    static constexpr uint32_t kTmemSlot = kBar + 8 * (kBStages + 10);   // tensor-memory address, abort flag
     static constexpr uint32_t kBytes = kTmemSlot + 16 + 1024;          // + alignment of the base
 };
 
@@ -155,15 +157,12 @@ template <int BN>
 __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constant__ GemmJob job)
 {
     using L = gemm::Layout<BN>;
-    constexpr int NC = BN / 32;                        // 32-column pieces of a partial
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const bool issuer = warp == gemm::kRowWarps;       // the warp that issues tensor copies and MMAs
+    constexpr int HN = BN / 2;                         // partial columns per folding thread
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x / job.ntn, nt = blockIdx.x - mt * job.ntn;
     const long long O = job.m.O;
     const long long o0 = (long long)mt * gemm::kBM;
     const int n0 = nt * BN;
-    const long long o = o0 + tid;                      // a row warp's thread: its weight row
-    const long long o_ld = o < O ? o : O - 1;          // rows past the end repeat the last one
     const int T = job.m.I / gemm::kBK;
     const int pbl = job.pbl;
     const int nbuf = pbl == 5 ? 4 : 2;                 // partial buffers in tensor memory
@@ -173,9 +172,12 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
     const uint32_t sbase = smem_base();
     const uint32_t off0 = ((sbase + 1023u) & ~1023u) - sbase;
     const uint32_t oA = off0 + L::kA, oB = off0 + L::kB, oRaw = off0 + L::kRaw, oScl = off0 + L::kScl;
-    const uint32_t bfull = sbase + off0 + L::kBar;                 // kBStages: x parts landed
-    const uint32_t afull = bfull + 8 * L::kBStages;                 // 2: decoded weight slab written
-    const uint32_t sdone = afull + 16;                              // 2: the MMAs of a step completed
+    const uint32_t oPs = off0 + L::kPScale;
+    const uint32_t bfull = sbase + off0 + L::kBar;     // kBStages: x parts landed (tensor copies)
+    const uint32_t afull = bfull + 8 * L::kBStages;     // 2: decoded weight slab written (decode warps)
+    const uint32_t sdone = afull + 16;                  // 2: the MMAs of a step completed (commit)
+    const uint32_t sfull = sdone + 16;                  // 4: a step's folding scales written (decode warps)
+    const uint32_t tfree = sfull + 32;                  // 2: a step's partials read (folding warps)
     const uint32_t tslot = sbase + off0 + L::kTmemSlot;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(reinterpret_cast<char*>(qg_smem4) + off0 +
                                                                L::kTmemSlot + 4);
@@ -183,8 +185,10 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
     if (warp == 0) tmem_alloc(tslot, ncols);
     if (tid == 0) {
         for (int i = 0; i < L::kBStages; i++) mbar_init(bfull + 8 * i, 1);
-        for (int i = 0; i < 2; i++) mbar_init(afull + 8 * i, gemm::kRowWarps);
+        for (int i = 0; i < 2; i++) mbar_init(afull + 8 * i, gemm::kDecodeWarps);
         for (int i = 0; i < 2; i++) mbar_init(sdone + 8 * i, 1);
+        for (int i = 0; i < 4; i++) mbar_init(sfull + 8 * i, gemm::kDecodeWarps);
+        for (int i = 0; i < 2; i++) mbar_init(tfree + 8 * i, gemm::kFoldWarps);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -194,9 +198,9 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
     const uint32_t tmem = lds_u32(off0 + L::kTmemSlot);
     bool failed_here = false;
 
-    if (issuer) {
-        // ---- one thread: tensor copies of the x parts, the MMAs, their commits ----
-        if ((tid & 31) == 0) {
+    if (warp >= gemm::kFoldWarps + gemm::kDecodeWarps) {
+        // ---- issue warp, one thread: tensor copies of the x parts, the MMAs ----
+        if (lane == 0) {
             auto issue_x = [&](int u) {
                 const uint32_t slot = u % L::kBStages;
                 const uint32_t bar = bfull + 8 * slot;
@@ -211,21 +215,26 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
             int t = 0;
             for (; t < T; t++) {
                 if (*abort_flag) break;
+                // the slab is decoded, the partial buffers of step t - 2 were read, x landed
                 if (!mbar_wait(afull + 8 * (t & 1), (uint32_t)(t >> 1) & 1u) ||
+                    (t >= 2 && !mbar_wait(tfree + 8 * (t & 1), (uint32_t)((t - 2) >> 1) & 1u)) ||
                     !mbar_wait(bfull + 8 * (t % L::kBStages), (uint32_t)(t / L::kBStages) & 1u)) {
                     failed_here = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sbase + oA + (t & 1) * gemm::kABytes;
-                const uint32_t bh = sbase + oB + (uint32_t)(t % L::kBStages) * L::kBBytes, bl = bh + BN * 128;
+                // descriptors of the step's slabs; a K step of 16 inputs is 32
+                // bytes further along the rows (+2 in the address field)
+                const uint64_t da = tc_desc_sw128(sbase + oA + (t & 1) * gemm::kABytes);
+                const uint64_t dh = tc_desc_sw128(sbase + oB + (uint32_t)(t % L::kBStages) * L::kBBytes);
+                const uint64_t dl = dh + (uint64_t)((BN * 128) >> 4);
 #pragma unroll
                 for (int j = 0; j < 4; j++) {
                     const int k = t * gemm::kBK + 16 * j;
                     const uint32_t d = tmem + (uint32_t)(((k >> pbl) % nbuf) * BN);
                     const uint32_t first = (k & ((1 << pbl) - 1)) == 0;
-                    tc_mma_f16(d, tc_desc_sw128(a0 + 32 * j), tc_desc_sw128(bh + 32 * j), idesc, first ? 0u : 1u);
-                    tc_mma_f16(d, tc_desc_sw128(a0 + 32 * j), tc_desc_sw128(bl + 32 * j), idesc, 1u);
+                    tc_mma_f16(d, da + 2 * j, dh + 2 * j, idesc, first ? 0u : 1u);
+                    tc_mma_f16(d, da + 2 * j, dl + 2 * j, idesc, 1u);
                 }
                 tc_commit(sdone + 8 * (t & 1));
                 // the x slot of step t - 1 is free once its MMAs are done: refill it
@@ -246,8 +255,11 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
                     mbar_wait(bfull + 8 * (u % L::kBStages), (uint32_t)(u / L::kBStages) & 1u);
             }
         }
-    } else {
-        // ---- row warps: weight decode, partial folding, the result ----
+    } else if (warp >= gemm::kFoldWarps) {
+        // ---- decode warps: weight row m; raw copies, scales, the f16 slab ----
+        const int m = (warp - gemm::kFoldWarps) * 32 + lane;
+        const long long o = o0 + m;
+        const long long o_ld = o < O ? o : O - 1;      // rows past the end repeat the last one
         const long long srow = o_ld * job.m.ngrp;      // first scale of the row
         float row_scale = 0.f;
         if constexpr (SK == SK_ROW) row_scale = ldg_f32(job.m.sc + o_ld);
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
         // the step (one commit group per step)
         auto issue_raw = [&](int u) {
             if (u < T) {
-                const uint32_t dst = sbase + oRaw + (uint32_t)(u % L::kRawStages) * gemm::kRawBytes + tid * 16;
+                const uint32_t dst = sbase + oRaw + (uint32_t)(u % L::kRawStages) * gemm::kRawBytes + m * 16;
                 if constexpr (FMT == FMT_INT8_ROW) {
 #pragma unroll
                     for (int c = 0; c < 4; c++)
@@ -276,7 +288,7 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
                         cp_async16(dst + c * gemm::kBM * 16, wrow + (long long)u * 32 + c * 16);
                 }
                 if constexpr (SK != SK_ROW) {
-                    const uint32_t sdst = sbase + oScl + (uint32_t)(u % L::kRawStages) * (gemm::kBM * 8) + tid * 8;
+                    const uint32_t sdst = sbase + oScl + (uint32_t)(u % L::kRawStages) * (gemm::kBM * 8) + m * 8;
                     if constexpr (SK == SK_E8M0) {
                         // groups 2u, 2u + 1: bytes of the aligned word that holds them
                         cp_async4(sdst, reinterpret_cast<const uint8_t*>(job.m.sc) + ((srow + 2ll * u) & ~3ll));
@@ -292,96 +304,108 @@ __global__ void __launch_bounds__(gemm::kThreads, 1) k_gemm(const __grid_constan
             cp_async_commit();
         };
         for (int u = 0; u < L::kRawStages - 1; u++) issue_raw(u);
-
-        float acc[BN];
-#pragma unroll
-        for (int n = 0; n < BN; n++) acc[n] = 0.f;
-        // folds the partial of block b (weight scale sc) into the sums
-        auto promote = [&](int b, float sc) {
-            const uint32_t col = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((b % nbuf) * BN);
-#pragma unroll
-            for (int c = 0; c < NC; c++) {
-                float v[32];
-                tmem_ld32(col + 32 * c, v);
-#pragma unroll
-                for (int i = 0; i < 32; i++) acc[32 * c + i] = fmaf(sc, v[i], acc[32 * c + i]);
-            }
-        };
-        float scp[2] = {0.f, 0.f};     // scales of the partials that ended in the previous step
-        int nprev = 0, bprev = 0;
-        int t = 0;
-        for (; t < T; t++) {
+        for (int t = 0; t < T; t++) {
             if (*abort_flag) break;
-            int nend, bend;
-            gemm_blocks_ending(t, T, pbl, nend, bend);
+            // A slot t % 2 is free once the MMAs of step t - 2 completed (that
+            // also bounds how far decoding runs ahead of the folding warps)
+            if (t >= 2 && !mbar_wait(sdone + 8 * (t & 1), (uint32_t)((t - 2) >> 1) & 1u)) {
+                failed_here = true;
+                break;
+            }
             cp_async_wait<L::kRawStages - 2>();
-            float scn[2];              // scales of the blocks ending in step t
+            // the scales of the blocks ending in step t, for the folding warps
+            float sc0, sc1;
             if constexpr (SK == SK_ROW) {
-                scn[0] = scn[1] = row_scale;
+                sc0 = sc1 = row_scale;
             } else {
-                const uint32_t so = oScl + (uint32_t)(t % L::kRawStages) * (gemm::kBM * 8) + tid * 8;
+                const uint32_t so = oScl + (uint32_t)(t % L::kRawStages) * (gemm::kBM * 8) + m * 8;
                 if constexpr (SK == SK_E8M0) {
                     const uint32_t wd = lds_u32(so), sh = (uint32_t)((2 * t) & 3);
-                    scn[0] = e8m0_to_f32(__byte_perm(wd, 0u, 0x4440u + sh));
-                    scn[1] = e8m0_to_f32(__byte_perm(wd, 0u, 0x4440u + sh + 1));
+                    sc0 = e8m0_to_f32(__byte_perm(wd, 0u, 0x4440u + sh));
+                    sc1 = e8m0_to_f32(__byte_perm(wd, 0u, 0x4440u + sh + 1));
                 } else if (pbl == 5) {
                     const uint2 v = lds8(so);
-                    scn[0] = __uint_as_float(v.x);
-                    scn[1] = __uint_as_float(v.y);
+                    sc0 = __uint_as_float(v.x);
+                    sc1 = __uint_as_float(v.y);
                 } else {
-                    scn[0] = scn[1] = lds_f32(so);
+                    sc0 = sc1 = lds_f32(so);
                 }
             }
-            // decode K step t into A slot t % 2 (its readers, the MMAs of step
-            // t - 2, completed: promote waited for them in the last step)
+            *reinterpret_cast<float2*>(reinterpret_cast<char*>(qg_smem4) + oPs + (t & 3) * (gemm::kBM * 8) + m * 8) =
+                make_float2(sc0, sc1);
             {
                 uint4 ch[8];
-                gemm_decode_step(oRaw + (uint32_t)(t % L::kRawStages) * gemm::kRawBytes + tid * 16, gemm::kBM * 16,
-                                 ch);
-                char* arow = reinterpret_cast<char*>(qg_smem4) + oA + (t & 1) * gemm::kABytes + (tid >> 3) * 1024 +
-                             (tid & 7) * 128;
+                gemm_decode_step(oRaw + (uint32_t)(t % L::kRawStages) * gemm::kRawBytes + m * 16, gemm::kBM * 16, ch);
+                char* arow = reinterpret_cast<char*>(qg_smem4) + oA + (t & 1) * gemm::kABytes + (m >> 3) * 1024 +
+                             (m & 7) * 128;
 #pragma unroll
-                for (int j = 0; j < 8; j++) *reinterpret_cast<uint4*>(arow + ((j ^ (tid & 7)) << 4)) = ch[j];
+                for (int j = 0; j < 8; j++) *reinterpret_cast<uint4*>(arow + ((j ^ (m & 7)) << 4)) = ch[j];
             }
             issue_raw(t + L::kRawStages - 1);
             fence_proxy_async_smem();
-            tc_fence_before();         // this thread's partial reads precede the arrival
             __syncwarp();
-            if ((tid & 31) == 0) mbar_arrive(afull + 8 * (t & 1));
-            // fold the partials that ended in step t - 1 while step t runs
-            if (t >= 1) {
-                if (!mbar_wait(sdone + 8 * ((t - 1) & 1), (uint32_t)((t - 1) >> 1) & 1u)) {
-                    failed_here = true;
-                    break;
-                }
-                tc_fence_after();
-                for (int i = 0; i < nprev; i++) promote(bprev + i, scp[i]);
-            }
-            nprev = nend;
-            bprev = bend;
-            scp[0] = scn[0];
-            scp[1] = scn[1];
-        }
-        // the last step's partials
-        if (!failed_here && t == T) {
-            if (!mbar_wait(sdone + 8 * ((T - 1) & 1), (uint32_t)((T - 1) >> 1) & 1u)) {
-                failed_here = true;
-            } else {
-                tc_fence_after();
-                for (int i = 0; i < nprev; i++) promote(bprev + i, scp[i]);
+            if (lane == 0) {
+                mbar_arrive(afull + 8 * (t & 1));
+                mbar_arrive(sfull + 8 * (t & 3));
             }
         }
         if (failed_here) *abort_flag = 1;
         cp_async_wait<0>();
-        tc_fence_before();
-        __syncwarp();
+    } else {
+        // ---- folding warps: lanes 32 q.. of tensor memory, column half hh ----
+        const int q = warp & 3, hh = warp >> 2;
+        const int m = q * 32 + lane;                   // weight row of this thread
+        const long long o = o0 + m;
+        float acc[HN];                                 // columns hh * HN .. hh * HN + HN - 1
+#pragma unroll
+        for (int n = 0; n < HN; n++) acc[n] = 0.f;
+        // folds this thread's columns of the partial of block b (weight scale
+        // sc) into its sums
+        auto promote = [&](int b, float sc) {
+            const uint32_t col = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((b % nbuf) * BN + hh * HN);
+            if constexpr (HN == 16) {
+                float v[16];
+                tmem_ld16(col, v);
+#pragma unroll
+                for (int i = 0; i < 16; i++) acc[i] = fmaf(sc, v[i], acc[i]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < HN / 32; c++) {
+                    float v[32];
+                    tmem_ld32(col + 32 * c, v);
+#pragma unroll
+                    for (int i = 0; i < 32; i++) acc[32 * c + i] = fmaf(sc, v[i], acc[32 * c + i]);
+                }
+            }
+        };
+        int t = 0;
+        for (; t < T; t++) {
+            if (*abort_flag) break;
+            if (!mbar_wait(sdone + 8 * (t & 1), (uint32_t)(t >> 1) & 1u) ||
+                !mbar_wait(sfull + 8 * (t & 3), (uint32_t)(t >> 2) & 1u)) {
+                failed_here = true;
+                break;
+            }
+            tc_fence_after();
+            int nend, bend;
+            gemm_blocks_ending(t, T, pbl, nend, bend);
+            const float2 sc = *reinterpret_cast<const float2*>(reinterpret_cast<const char*>(qg_smem4) + oPs +
+                                                                (t & 3) * (gemm::kBM * 8) + m * 8);
+            if (nend > 0) promote(bend, sc.x);
+            if (nend > 1) promote(bend + 1, sc.y);
+            tc_fence_before();         // the partial reads precede the arrival
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tfree + 8 * (t & 1));
+        }
+        if (failed_here) *abort_flag = 1;
         // y[n][o] = sum * 2^-pexp[n]
         if (!failed_here && t == T && o < O) {
 #pragma unroll
-            for (int n = 0; n < BN; n++) {
-                if (n0 + n < job.s) {
-                    const int p = job.pexp[n0 + n];
-                    job.y[(long long)(n0 + n) * O + o] = acc[n] * __uint_as_float((uint32_t)(127 - p) << 23);
+            for (int i = 0; i < HN; i++) {
+                const int n = n0 + hh * HN + i;
+                if (n < job.s) {
+                    const int p = job.pexp[n];
+                    job.y[(long long)n * O + o] = acc[i] * __uint_as_float((uint32_t)(127 - p) << 23);
                 }
             }
         }

@@ -141,6 +141,7 @@ class GemvWorkload:
     scale_mu: float
     seed: int
     x_key: int = 0
+    gemm: bool = False      # a prefill batch, run through the tensor-core GEMM
 
     @property
     def weight_bytes(self) -> int:
@@ -278,6 +279,13 @@ def workload(name: str):
         "mxfp4_e8m0_experts_E256_D6144_F2048_s1_k8": ExpertWorkload("mxfp4_e8m0_experts_E256_D6144_F2048_s1_k8",
                                                                     MXFP4_E8M0, 256, 6144, 2048, 1, 8, 32,
                                                                     "pow2", 0.0, 1004),
+        # Prefill batches through the tensor-core GEMM: the int4-g32 matrix with
+        # 512 activation rows (the pages' prefill measurements use 512-row
+        # prompts) and with 32 (the engines' default prefill chunk).
+        "int4_g32_16384x6144_s512_prefill": GemvWorkload("int4_g32_16384x6144_s512_prefill", INT4_G, 16384, 6144,
+                                                         512, 32, "lognormal", -4.0, 1002, x_key=512, gemm=True),
+        "int4_g32_16384x6144_s32_prefill": GemvWorkload("int4_g32_16384x6144_s32_prefill", INT4_G, 16384, 6144,
+                                                        32, 32, "lognormal", -4.0, 1002, x_key=32, gemm=True),
     }
     return table[name]
 
@@ -297,4 +305,10 @@ VARIANT_WORKLOADS = [
     "int4_row_16384x6144_s1",
     "int8_g64_16384x6144_s1",
     "mxfp4_e8m0_experts_E256_D6144_F2048_s1_k8",
+]
+
+# Prefill workloads (the tensor-core GEMM).
+PREFILL_WORKLOADS = [
+    "int4_g32_16384x6144_s512_prefill",
+    "int4_g32_16384x6144_s32_prefill",
 ]
