@@ -337,6 +337,71 @@ void oracle_expert_group_cols(int fmt, long gs,
                                  0.0, cols, ncols, out, h_scratch);
 }
 
+/* ------------------------------------------------------------------------
+ * The router ([VULKAN] the per-engine host steps: "the router's softmax and
+ * top-k" for the softmax models; "sigmoid scores, the correction bias picks,
+ * top-k renormalized" for the sigmoid-router models).  Per token t, over its
+ * E logits l[t][e]:
+ *   kind 0 (softmax): score p_e = exp(l_e) / sum_j exp(l_j); the k largest
+ *          p_e are chosen; weight = p_e, or with renorm p_e / sum over the
+ *          chosen of p.
+ *   kind 1 (sigmoid with correction bias): score s_e = 1 / (1 + exp(-l_e));
+ *          the k largest s_e + bias_e are chosen; weight = s_e, or with
+ *          renorm s_e / sum over the chosen of s.
+ * Every weight is then multiplied by `scale` (the models' routed scaling
+ * factor; 1 for none).  Readings where the pages are silent: ranks are in
+ * decreasing selection key, equal keys rank the lower expert index first.
+ * Selection for kind 0 compares the logits themselves (exp is increasing, so
+ * that is the same choice as comparing p); kind 1 compares s_e + bias_e in
+ * double.  Outputs ids[t][r], wts[t][r] for rank r < k.
+ * ------------------------------------------------------------------------ */
+double oracle_sigmoid(double z)
+{
+    return 1.0 / (1.0 + exp(-z));
+}
+
+void oracle_route(int kind, const float *logits, const float *bias, long s, long E, long k, int renorm,
+                  double scale, int32_t *ids, double *wts, double *key_scratch, unsigned char *taken)
+{
+    for (long t = 0; t < s; t++) {
+        const float *l = logits + t * E;
+        for (long e = 0; e < E; e++) {
+            key_scratch[e] = kind == 0 ? (double)l[e] : oracle_sigmoid((double)l[e]) + (double)bias[e];
+            taken[e] = 0;
+        }
+        /* top k: repeatedly the largest remaining key, lowest index on ties */
+        for (long r = 0; r < k; r++) {
+            long best = -1;
+            for (long e = 0; e < E; e++) {
+                if (taken[e]) continue;
+                if (best < 0 || key_scratch[e] > key_scratch[best]) best = e;
+            }
+            taken[best] = 1;
+            ids[t * k + r] = (int32_t)best;
+        }
+        /* weights */
+        double denom = 0.0;
+        if (kind == 0) {
+            double mx = -INFINITY;
+            for (long e = 0; e < E; e++) mx = l[e] > mx ? l[e] : mx;
+            if (renorm) {
+                for (long r = 0; r < k; r++) denom += exp((double)l[ids[t * k + r]] - mx);
+            } else {
+                for (long e = 0; e < E; e++) denom += exp((double)l[e] - mx);
+            }
+            for (long r = 0; r < k; r++)
+                wts[t * k + r] = scale * exp((double)l[ids[t * k + r]] - mx) / denom;
+        } else {
+            if (renorm)
+                for (long r = 0; r < k; r++) denom += oracle_sigmoid((double)l[ids[t * k + r]]);
+            for (long r = 0; r < k; r++) {
+                const double sg = oracle_sigmoid((double)l[ids[t * k + r]]);
+                wts[t * k + r] = scale * (renorm ? sg / denom : sg);
+            }
+        }
+    }
+}
+
 /* Number of threads the OpenMP loops above use (1 when built without it). */
 int oracle_threads(void)
 {

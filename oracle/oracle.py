@@ -94,6 +94,9 @@ class Oracle:
         lib.oracle_qgate_up.argtypes = [I, L, P, P, P, P, P, L, L, L, P]
         lib.oracle_qgate_up_rows.argtypes = [I, L, P, P, P, P, P, L, L, L, P, L, P]
         lib.oracle_expert_group_cols.argtypes = [I, L, P, P, P, P, P, P, L, L, L, P, L, L, P, P, P, L, P, P]
+        lib.oracle_sigmoid.argtypes = [D]
+        lib.oracle_sigmoid.restype = D
+        lib.oracle_route.argtypes = [I, P, P, L, L, L, I, D, P, P, P, P]
         lib.oracle_threads.restype = I
         self.lib = lib
 
@@ -196,6 +199,23 @@ class Oracle:
         return out
 
 
+    def sigmoid(self, z: float) -> float:
+        return self.lib.oracle_sigmoid(float(z))
+
+    def route(self, kind: int, logits, bias=None, k: int = 8, renorm: bool = True, scale: float = 1.0):
+        """(ids int32 [s][k], weights double [s][k]) of the router (kind 0 softmax, 1 sigmoid + bias)."""
+        logits = _f32(logits)
+        s, E = logits.shape
+        b = _f32(np.zeros(E) if bias is None else bias)
+        ids = np.empty((s, k), dtype=np.int32)
+        w = np.empty((s, k), dtype=np.float64)
+        keys = np.empty(E, dtype=np.float64)
+        taken = np.empty(E, dtype=np.uint8)
+        self.lib.oracle_route(int(kind), _p(logits), _p(b), s, E, k, int(bool(renorm)), float(scale), _p(ids),
+                              _p(w), _p(keys), _p(taken))
+        return ids, w
+
+
 _default: Oracle | None = None
 
 
@@ -210,6 +230,6 @@ def default() -> Oracle:
 def __getattr__(name):
     # Module-level access to the default copy's methods: oracle.qgemv(...), ...
     if name in {"threads", "packed_bytes", "codes", "e2m1", "code_value", "e8m0", "silu", "glu", "dequant_f32",
-                "qgemv", "qgemv_rows", "qgate_up", "qgate_up_rows", "expert_group"}:
+                "qgemv", "qgemv_rows", "qgate_up", "qgate_up_rows", "expert_group", "sigmoid", "route"}:
         return getattr(default(), name)
     raise AttributeError(name)

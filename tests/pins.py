@@ -391,7 +391,68 @@ def pin_expert_group(orc):
         assert not orc.expert_group(fmt, gs, *packed, E, D, F, x, ids, wts, act=1, limit=0.0).any()
 
 
+# --- the router (softmax / sigmoid-with-bias top-k) -------------------------
+
+def pin_route_selection(orc):
+    """Hand-built keys: the k largest in decreasing order, equal keys lower index first."""
+    l = np.array([[1.0, 3.0, 3.0, 2.0, 3.0]], dtype=np.float32)
+    assert orc.route(0, l, k=3)[0].tolist() == [[1, 2, 4]]
+    assert orc.route(0, l, k=4)[0].tolist() == [[1, 2, 4, 3]]
+    assert orc.route(0, l, k=5)[0].tolist() == [[1, 2, 4, 3, 0]]
+    # the chosen set is the k largest on random rows (any k), ranks in decreasing logit
+    rng = np.random.default_rng(53)
+    L = rng.standard_normal((20, 64)).astype(np.float32)
+    for k in (1, 4, 8, 64):
+        ids, _ = orc.route(0, L, k=k)
+        for t in range(20):
+            want = np.argsort(-L[t].astype(np.float64), kind="stable")[:k]
+            assert ids[t].tolist() == want.tolist()
+
+
+def pin_route_softmax_weights(orc):
+    """Softmax closed forms: ratios exp(l_i - l_j), a full set sums to 1, shift invariance, renorm."""
+    rng = np.random.default_rng(59)
+    L = (np.round(3 * rng.standard_normal((6, 32)) * 64) / 64).astype(np.float32)   # exact under + 4
+    ids, w = orc.route(0, L, k=32, renorm=False)
+    _close(w.sum(axis=1), np.ones(6), rtol=1e-14)
+    for t in range(6):
+        li = L[t, ids[t]].astype(np.float64)
+        _close(w[t] / w[t, 0], np.exp(li - li[0]), rtol=1e-13)
+    ids8, w8 = orc.route(0, L, k=8, renorm=False)
+    _close(w8, w[:, :8], rtol=1e-14)                          # the same p, just fewer of them
+    ids8r, w8r = orc.route(0, L, k=8, renorm=True, scale=2.5)
+    _close(w8r, 2.5 * w8 / w8.sum(axis=1, keepdims=True), rtol=1e-14)
+    assert (ids8r == ids8).all()
+    _, ws = orc.route(0, L + np.float32(4.0), k=8, renorm=False)   # exact shift of every logit
+    _close(ws, w8, rtol=1e-12)
+    # equal logits: uniform
+    _, wu = orc.route(0, np.zeros((1, 16), np.float32), k=16, renorm=False)
+    _close(wu, np.full((1, 16), 1 / 16), rtol=1e-15)
+
+
+def pin_route_sigmoid_bias(orc):
+    """Sigmoid router: the bias picks, the unbiased scores weigh."""
+    assert orc.sigmoid(0.0) == 0.5
+    _close(orc.sigmoid(1.5) + orc.sigmoid(-1.5), 1.0, rtol=1e-15)
+    _close(orc.sigmoid(2.0), 1 / (1 + np.exp(-2.0)), rtol=1e-15)
+    l = np.zeros((1, 4), np.float32)
+    b = np.array([0.0, 0.1, 0.0, 0.2], np.float32)
+    ids, w = orc.route(1, l, b, k=2, renorm=False, scale=3.0)
+    assert ids.tolist() == [[3, 1]]
+    _close(w, [[1.5, 1.5]], rtol=1e-15)                         # 3 * sigmoid(0), bias not in the weight
+    ids, w = orc.route(1, l, b, k=2, renorm=True)
+    _close(w, [[0.5, 0.5]], rtol=1e-15)
+    # a bias large enough overrides the logits; without bias the order follows the logits
+    l2 = np.array([[2.0, -1.0, 0.5]], np.float32)
+    assert orc.route(1, l2, np.zeros(3, np.float32), k=3)[0].tolist() == [[0, 2, 1]]
+    assert orc.route(1, l2, np.array([0, 5, 0], np.float32), k=1)[0].tolist() == [[1]]
+    ids, w = orc.route(1, l2, np.zeros(3, np.float32), k=2, renorm=True)
+    s0, s2 = 1 / (1 + np.exp(-2.0)), 1 / (1 + np.exp(-0.5))
+    _close(w, [[s0 / (s0 + s2), s2 / (s0 + s2)]], rtol=1e-14)
+
+
 ALL_PINS = [pin_e2m1, pin_e8m0, pin_int4_nibbles, pin_int3_planes, pin_int8_bytes, pin_random_codes,
             pin_format_variants,
             pin_dequant_f32, pin_fixed_groups, pin_gemv_bruteforce, pin_zero_scales, pin_linearity,
-            pin_integer_exact, pin_silu, pin_clamped_glu, pin_gate_up, pin_gate_up_clamped, pin_expert_group]
+            pin_integer_exact, pin_silu, pin_clamped_glu, pin_gate_up, pin_gate_up_clamped, pin_expert_group,
+            pin_route_selection, pin_route_softmax_weights, pin_route_sigmoid_bias]

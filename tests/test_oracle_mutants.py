@@ -44,6 +44,13 @@ MUTANTS = {
     "int4_row_no_offset": ("case ORACLE_INT4_ROW:\n    case ORACLE_INT4_G: return (double)(code - 8);",
                            "case ORACLE_INT4_G: return (double)(code - 8);\n    case ORACLE_INT4_ROW: return (double)code;"),
     "expert_rank_last_only": ("out[t * ncols + j] = 0.0;", "out[t * ncols + j] = 0.0 * out[t * ncols + j];"),
+    "route_ties_high_index": ("key_scratch[e] > key_scratch[best]) best = e;", "key_scratch[e] >= key_scratch[best]) best = e;"),
+    "route_renorm_over_all": ("if (renorm) {\n                for (long r = 0; r < k; r++) denom +=",
+                              "if (0) {\n                for (long r = 0; r < k; r++) denom +="),
+    "route_bias_in_weight": ("const double sg = oracle_sigmoid((double)l[ids[t * k + r]]);",
+                             "const double sg = oracle_sigmoid((double)l[ids[t * k + r]]) + (double)bias[ids[t * k + r]];"),
+    "route_sigmoid_sign": ("return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
+    "route_scale_dropped": ("wts[t * k + r] = scale * exp(", "wts[t * k + r] = exp("),
 }
 
 
