@@ -97,7 +97,8 @@ enum {
     QSTATUS_LAUNCH = -6,         /* CUDA reported an error at launch */
     QSTATUS_DEVICE_TIMEOUT = -7, /* a bounded device-side wait ran out */
     QSTATUS_BAD_EXPERT_ID = -8,  /* an expert id outside [0, E) (reported on the device) */
-    QSTATUS_BAD_ACT = -9         /* unknown activation, or a limit that is negative or NaN */
+    QSTATUS_BAD_ACT = -9,        /* unknown activation, or a limit that is negative or NaN */
+    QSTATUS_BAD_ROUTE = -10      /* unknown router kind, or a NaN router scale */
 };
 
 /*
@@ -242,6 +243,48 @@ size_t qgemm_workspace(int I, int s);
 int qgemm(int fmt, int gs, const void* w, const float* scales,
           const float* x, int O, int I, int s, float* y,
           void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The router on the device: for each token t < s, the k of E experts with the
+ * largest keys and their weights, from the router logits -- the step
+ * colibri's engines run on the host (docs/vulkan.md, the per-engine host-step
+ * tables: the softmax routers' "softmax and top-k"; the sigmoid routers'
+ * scores, correction-bias picks and renormalized top-k).
+ *   QROUTE_SOFTMAX       key = logit (the same order as the softmax
+ *                        probability); weight = the probability
+ *                        exp(l_e) / sum_j exp(l_j) over all E experts, or with
+ *                        renorm != 0 over the k chosen.
+ *   QROUTE_SIGMOID_BIAS  key = sigmoid(logit) + bias[e]; weight = sigmoid(logit),
+ *                        divided by the sum over the k chosen if renorm != 0.
+ * Every weight is multiplied by `scale` (a routed scaling factor; 1 for none).
+ * Ranks run in decreasing key; equal keys rank the lower expert index first; a
+ * NaN key ranks below every number.
+ *   logits f32 [s][E];  bias f32 [E] (QROUTE_SIGMOID_BIAS only, else may be
+ *   NULL);  ids int32 [s][k] and wts f32 [s][k], written in rank order.
+ * 1 <= k <= 32, k <= E <= 1024.  QSTATUS_BAD_ROUTE for an unknown kind or a
+ * NaN scale.
+ */
+#define QROUTE_SOFTMAX 0
+#define QROUTE_SIGMOID_BIAS 1
+int qroute(int kind, const float* logits, const float* bias, int s, int E, int k, int renorm, float scale,
+           int32_t* ids, float* wts, void* stream);
+
+/*
+ * qroute followed by qexpert_group_act in one call: the routing is written to
+ * ids_out / wts_out (device int32 / f32 [s][k], caller-owned) and the expert
+ * group reads it from there; the expert launches wait for the router on the
+ * device (no host round trip).  Arguments and statuses as for the two calls.
+ */
+int qexpert_group_routed(int fmt, int gs,
+                         const void* gate, const float* gate_s,
+                         const void* up, const float* up_s,
+                         const void* down, const float* down_s,
+                         int E, int D, int F,
+                         const float* x, int s, int k,
+                         int route_kind, const float* logits, const float* bias, int renorm, float route_scale,
+                         int act, float limit,
+                         float* out, int32_t* ids_out, float* wts_out,
+                         void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /* A static description of a status code. */
 const char* qstatus_string(int status);

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for st in range(0, -10, -1):
+    for st in range(0, -11, -1):
         assert _lib.qstatus_string(st) and "unknown status" not in _lib.qstatus_string(st)
     assert "unknown" in _lib.qstatus_string(-100)
 
@@ -156,3 +156,28 @@ def test_qgemm_checks(L):
     assert L.qgemm(4, 32, A, A, A, 16, 6144, 512, A, None, ws, None) == -4   # no workspace
     assert L.qgemm(4, 32, A, A, A, 16, 6144, 512, A, A + 16, ws, None) == -3  # workspace not 256-aligned
     assert L.qgemm(4, 32, A, A, A, 16, 6144, 0, A, A, ws, None) == -2       # s < 1
+
+
+def test_route_checks(L):
+    """qroute / qexpert_group_routed host-side checks (nothing is enqueued)."""
+    f = ctypes.c_float
+    L.qroute.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 4 + \
+        [f, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.qroute(2, A, A, 4, 256, 8, 1, 1.0, A, A, None) == -10            # unknown kind
+    assert L.qroute(0, A, A, 4, 256, 8, 1, float("nan"), A, A, None) == -10   # NaN scale
+    assert L.qroute(0, A, None, 4, 256, 33, 1, 1.0, A, A, None) == -2         # k above 32
+    assert L.qroute(0, A, None, 4, 8, 9, 1, 1.0, A, A, None) == -2            # k above E
+    assert L.qroute(0, A, None, 4, 1025, 8, 1, 1.0, A, A, None) == -2         # E above 1024
+    assert L.qroute(0, A, None, 0, 256, 8, 1, 1.0, A, A, None) == -2          # no tokens
+    assert L.qroute(1, A, None, 4, 256, 8, 1, 1.0, A, A, None) == -4          # sigmoid router needs a bias
+    assert L.qroute(0, A + 2, None, 4, 256, 8, 1, 1.0, A, A, None) == -3      # misaligned logits
+    Z = ctypes.c_size_t
+    L.qexpert_group_routed.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 6 + [ctypes.c_int] * 3 + \
+        [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+         f, ctypes.c_int, f, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, Z, ctypes.c_void_p,
+         ctypes.c_void_p]
+    ws = _lib.lib().qexpert_group_workspace(256, 6144, 2048, 8, 8)
+    base = [7, 0, A, A, A, A, A, A, 256, 6144, 2048, A, 8, 8]
+    assert L.qexpert_group_routed(*base, 2, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws, None, None) == -10
+    assert L.qexpert_group_routed(*base, 0, A, None, 1, 1.0, 5, 0.0, A, A, A, A, ws, None, None) == -9
+    assert L.qexpert_group_routed(*base, 0, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws - 1, None, None) == -5

@@ -1,0 +1,108 @@
+"""The router on the GPU (qroute, qexpert_group_routed) against the oracle.
+
+Softmax routing selects by the logits themselves, so its ids must equal the
+oracle's exactly (ties: lower index first); sigmoid routing selects by f32
+keys sigmoid(l) + bias, which equal the oracle's f64 keys up to rounding, so
+its ids are held to the oracle's on random logits (gaps far above the
+rounding) and to validity (every chosen key at least every unchosen one, up
+to the rounding) on top.  Weights: within 1e-6 of the oracle's.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import GATE, MXFP4_G32, INT4_G, cuda, dev, empty_f32, host, max_rel, torch
+from oracle import oracle
+from test_gpu_expert_group import small_store
+from weight_only_quantized_qgemv_gb300 import (QACT_SWIGLU, QROUTE_SIGMOID_BIAS, QROUTE_SOFTMAX, qexpert_group_act,
+                                               qexpert_group_routed, qexpert_group_workspace, qroute, synth)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_route(kind, logits, bias, k, renorm, scale):
+    s, E = logits.shape
+    ids = torch.empty((s, k), dtype=torch.int32, device=cuda())
+    wts = torch.empty((s, k), dtype=torch.float32, device=cuda())
+    qroute(kind, dev(logits), None if bias is None else dev(bias), s, E, k, renorm, scale, ids, wts)
+    return host(ids), host(wts)
+
+
+@pytest.mark.parametrize("E,k", [(8, 1), (8, 8), (64, 4), (256, 8), (256, 32), (1000, 6)])
+@pytest.mark.parametrize("s", [1, 37])
+@pytest.mark.parametrize("renorm,scale", [(0, 1.0), (1, 1.0), (1, 2.5)])
+def test_route_softmax(E, k, s, renorm, scale):
+    rng = synth.generator(181, E, k, s)
+    logits = (2 * rng.standard_normal((s, E))).astype(np.float32)
+    ids, w = run_route(QROUTE_SOFTMAX, logits, None, k, renorm, scale)
+    want_ids, want_w = oracle.route(0, logits, k=k, renorm=bool(renorm), scale=scale)
+    assert np.array_equal(ids, want_ids)
+    assert np.abs(w - want_w).max() <= 1e-6 * np.abs(want_w).max()
+
+
+@pytest.mark.parametrize("E,k", [(64, 4), (256, 8), (256, 32)])
+@pytest.mark.parametrize("renorm,scale", [(0, 1.0), (1, 2.5)])
+def test_route_sigmoid_bias(E, k, renorm, scale):
+    s = 29
+    rng = synth.generator(191, E, k)
+    logits = (2 * rng.standard_normal((s, E))).astype(np.float32)
+    bias = (0.2 * rng.standard_normal(E)).astype(np.float32)
+    ids, w = run_route(QROUTE_SIGMOID_BIAS, logits, bias, k, renorm, scale)
+    want_ids, want_w = oracle.route(1, logits, bias, k=k, renorm=bool(renorm), scale=scale)
+    keys = 1 / (1 + np.exp(-logits.astype(np.float64))) + bias.astype(np.float64)
+    for t in range(s):
+        chosen = keys[t, ids[t]]
+        rest = np.delete(keys[t], ids[t])
+        assert len(set(ids[t].tolist())) == k
+        assert chosen.min() >= rest.max() - 1e-6 and np.all(np.diff(chosen) <= 1e-6)
+    assert np.array_equal(ids, want_ids)
+    assert np.abs(w - want_w).max() <= 1e-6 * np.abs(want_w).max()
+
+
+def test_route_ties_and_nan():
+    """Equal keys: lower index first; NaN logits rank last."""
+    E, k = 64, 8
+    z = np.zeros((2, E), dtype=np.float32)
+    z[1, 3] = np.nan
+    z[1, 0] = np.nan
+    ids, w = run_route(QROUTE_SOFTMAX, z, None, k, 1, 1.0)
+    assert ids[0].tolist() == list(range(k))
+    assert ids[1].tolist() == [1, 2, 4, 5, 6, 7, 8, 9]
+    assert np.allclose(w, 1.0 / k)
+    lg = np.full((1, E), -1.0, dtype=np.float32)
+    lg[0, 10] = lg[0, 20] = 2.0
+    ids, _ = run_route(QROUTE_SIGMOID_BIAS, lg, np.zeros(E, np.float32), 3, 1, 1.0)
+    assert ids[0].tolist() == [10, 20, 0]
+
+
+@pytest.mark.parametrize("fmt,gs", [(MXFP4_G32, 0), (INT4_G, 32)])
+@pytest.mark.parametrize("kind", [QROUTE_SOFTMAX, QROUTE_SIGMOID_BIAS])
+def test_expert_group_routed(fmt, gs, kind):
+    """Routing and the expert group in one call: the two calls' bits, and the oracle's result."""
+    E, D, F, s, k = 16, 256, 128, 5, 4
+    st = small_store(fmt, E, D, F, 193)
+    rng = synth.generator(197, fmt, kind)
+    x = synth.draw_x(s, D, rng)
+    logits = rng.standard_normal((s, E)).astype(np.float32)
+    bias = (0.3 * rng.standard_normal(E)).astype(np.float32)
+    d = {n: dev(v) for n, v in st.items()}
+    ws_bytes = qexpert_group_workspace(E, D, F, s, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
+    out = empty_f32(s, D)
+    ids = torch.empty((s, k), dtype=torch.int32, device=cuda())
+    wts = torch.empty((s, k), dtype=torch.float32, device=cuda())
+    qexpert_group_routed(fmt, gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], E, D, F,
+                         dev(x), s, k, kind, dev(logits), dev(bias), 1, 1.0, QACT_SWIGLU, 0.0, out, ids, wts, ws,
+                         ws_bytes, status)
+    assert int(host(status)[0]) == 0
+    want_ids, want_w = oracle.route(kind, logits, bias, k=k, renorm=True)
+    assert np.array_equal(host(ids), want_ids)
+    # the same expert group from the two separate calls
+    out2 = empty_f32(s, D)
+    qexpert_group_act(fmt, gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], E, D, F, dev(x),
+                      s, k, ids, wts, QACT_SWIGLU, 0.0, out2, ws, ws_bytes, status)
+    assert np.array_equal(host(out).view(np.uint32), host(out2).view(np.uint32))
+    g = synth.fixed_group(fmt, D, gs or None)
+    want = oracle.expert_group(fmt, g, st["gate"], st["gate_s"], st["up"], st["up_s"], st["down"], st["down_s"],
+                               E, D, F, x, want_ids, want_w.astype(np.float32))
+    assert max_rel(host(out), want) <= GATE

@@ -27,9 +27,11 @@ QSTATUS = {
     -7: "QSTATUS_DEVICE_TIMEOUT",
     -8: "QSTATUS_BAD_EXPERT_ID",
     -9: "QSTATUS_BAD_ACT",
+    -10: "QSTATUS_BAD_ROUTE",
 }
 
 QACT_SWIGLU, QACT_SWIGLU_CLAMPED = 0, 1
+QROUTE_SOFTMAX, QROUTE_SIGMOID_BIAS = 0, 1
 
 
 class QStatusError(RuntimeError):
@@ -68,6 +70,11 @@ def lib() -> ctypes.CDLL:
         L.qgate_up_act.restype = I
         L.qexpert_group_act.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, P, P, I, Fl, P, P, Z, P, P]
         L.qexpert_group_act.restype = I
+        L.qroute.argtypes = [I, P, P, I, I, I, I, Fl, P, P, P]
+        L.qroute.restype = I
+        L.qexpert_group_routed.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, I, P, P, I, Fl, I, Fl, P, P, P,
+                                           P, Z, P, P]
+        L.qexpert_group_routed.restype = I
         L.qgemm_workspace.argtypes = [I, I]
         L.qgemm_workspace.restype = Z
         L.qgemm.argtypes = [I, I, P, P, P, I, I, I, P, P, Z, P]
@@ -164,6 +171,21 @@ def qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x,
                                    _ptr(down_s), E, D, F, _ptr(x), s, k, _ptr(ids), _ptr(wts), int(act),
                                    float(limit), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status_dev),
                                    _stream(stream)))
+
+
+def qroute(kind, logits, bias, s, E, k, renorm, scale, ids, wts, stream=None):
+    _check(lib().qroute(int(kind), _ptr(logits), _ptr(bias), s, E, k, int(renorm), float(scale), _ptr(ids), _ptr(wts),
+                        _stream(stream)))
+
+
+def qexpert_group_routed(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, route_kind, logits, bias,
+                         renorm, route_scale, act, limit, out, ids_out, wts_out, workspace, ws_bytes,
+                         status_dev=None, stream=None):
+    _check(lib().qexpert_group_routed(fmt, gs, _ptr(gate), _ptr(gate_s), _ptr(up), _ptr(up_s), _ptr(down),
+                                      _ptr(down_s), E, D, F, _ptr(x), s, k, int(route_kind), _ptr(logits), _ptr(bias),
+                                      int(renorm), float(route_scale), int(act), float(limit), _ptr(out),
+                                      _ptr(ids_out), _ptr(wts_out), _ptr(workspace), int(ws_bytes),
+                                      _ptr(status_dev), _stream(stream)))
 
 
 def qgemm_workspace(I, s) -> int:

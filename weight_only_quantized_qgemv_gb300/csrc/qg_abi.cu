@@ -329,6 +329,7 @@ const char* qstatus_string(int status)
     case QSTATUS_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case QSTATUS_BAD_EXPERT_ID: return "an expert id is outside [0, E)";
     case QSTATUS_BAD_ACT: return "unknown activation, or a clamp limit that is negative or NaN";
+    case QSTATUS_BAD_ROUTE: return "unknown router kind, or a NaN router scale";
     default: return "unknown status";
     }
 }
@@ -502,6 +503,39 @@ int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, co
     e = expert_combine(a, cs);
     if (e != cudaSuccess) return launch_status(e);
     return QSTATUS_OK;
+}
+
+int qroute(int kind, const float* logits, const float* bias, int s, int E, int k, int renorm, float scale,
+           int32_t* ids, float* wts, void* stream)
+{
+    if ((kind != QROUTE_SOFTMAX && kind != QROUTE_SIGMOID_BIAS) || !(scale == scale)) return QSTATUS_BAD_ROUTE;
+    if (s < 1 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) return QSTATUS_BAD_DIM;
+    if (!logits || !ids || !wts || (kind == QROUTE_SIGMOID_BIAS && !bias)) return QSTATUS_NULL;
+    if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(wts, 4) || (bias && !aligned(bias, 4)))
+        return QSTATUS_MISALIGNED;
+    return launch_status(route_launch(kind, logits, kind == QROUTE_SIGMOID_BIAS ? bias : nullptr, s, E, k,
+                                      renorm != 0, scale, ids, wts, static_cast<cudaStream_t>(stream)));
+}
+
+int qexpert_group_routed(int fmt, int gs, const void* gate, const float* gate_s, const void* up, const float* up_s,
+                         const void* down, const float* down_s, int E, int D, int F, const float* x, int s, int k,
+                         int route_kind, const float* logits, const float* bias, int renorm, float route_scale,
+                         int act, float limit, float* out, int32_t* ids_out, float* wts_out, void* workspace,
+                         size_t ws_bytes, int32_t* status_dev, void* stream)
+{
+    // every host-side check of the expert group first, so a rejected call enqueues nothing
+    int g = 0;
+    int st = check_act(act, limit);
+    if (st) return st;
+    if ((st = check_fmt(fmt, gs, D, &g)) || (st = check_fmt(fmt, gs, F, &g))) return st;
+    if (E < 1 || D < 1 || F < 1 || s < 1 || k < 1 || D > kMaxI || F > kMaxI) return QSTATUS_BAD_DIM;
+    if ((long long)s * k > kMaxPairs) return QSTATUS_BAD_DIM;
+    if (!workspace) return QSTATUS_NULL;
+    if (ws_bytes < ws_layout(D, F, s, k).total) return QSTATUS_WORKSPACE;
+    st = qroute(route_kind, logits, bias, s, E, k, renorm, route_scale, ids_out, wts_out, stream);
+    if (st) return st;
+    return qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids_out, wts_out, act,
+                             limit, out, workspace, ws_bytes, status_dev, stream);
 }
 
 size_t qgemm_workspace(int I, int s)

@@ -152,6 +152,10 @@ bool encode_x_map(CUtensorMap* map, const void* base, long long rows, long long 
 cudaError_t gemm_split_x(const float* x, int s, int sp, int I, int perm, void* xh, void* xl, int32_t* pexp,
                          cudaStream_t st);
 
+// The router kernel (qg_route.cu).
+cudaError_t route_launch(int kind, const float* logits, const float* bias, int s, int E, int k, int renorm,
+                         float scale, int32_t* ids, float* wts, cudaStream_t st);
+
 // Per-format launchers (defined in qg_fmt_<format>.cu).  Each returns a
 // cudaError_t of the launch.
 #define QG_DECLARE_FMT(name)                                                                            \
