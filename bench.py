@@ -248,7 +248,7 @@ class GemvBench:
 
 
 class ExpertBench:
-    def __init__(self, wl, device, nsteps, swiglu_limit=None):
+    def __init__(self, wl, device, nsteps, swiglu_limit=None, device_route=False):
         import torch
         from weight_only_quantized_qgemv_gb300 import QACT_SWIGLU, QACT_SWIGLU_CLAMPED, qexpert_group_workspace
         self.wl = wl
@@ -290,10 +290,26 @@ class ExpertBench:
         self.expert_bytes = wl.expert_bytes()
         self.route_bytes = [len(np.unique(self.ids_host[r])) * self.expert_bytes for r in range(self.nroutes)]
         self.launches_per_step = 4
+        self.device_route = device_route
+        if device_route:
+            # routing on the device from seeded logits: softmax top-k, renormalized
+            self.logits_host = np.stack([wl.router_logits(step=r) for r in range(self.nroutes)])
+            self.logits = torch.from_numpy(self.logits_host).to(device)
+            self.ids_out = torch.empty(wl.s, wl.k, dtype=torch.int32, device=device)
+            self.wts_out = torch.empty(wl.s, wl.k, dtype=torch.float32, device=device)
+            top = np.argpartition(-self.logits_host, wl.k - 1, axis=2)[:, :, :wl.k]
+            self.route_bytes = [len(np.unique(top[r])) * self.expert_bytes for r in range(self.nroutes)]
+            self.launches_per_step = 5
 
-    def _call(self, r, x, ids, wts, stream):
-        from weight_only_quantized_qgemv_gb300 import qexpert_group_act
+    def _call(self, r, x, ids, wts, stream, logits=None):
+        from weight_only_quantized_qgemv_gb300 import QROUTE_SOFTMAX, qexpert_group_act, qexpert_group_routed
         wl, d = self.wl, self.d
+        if self.device_route:
+            qexpert_group_routed(wl.fmt, self.gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"],
+                                 wl.E, wl.D, wl.F, x, wl.s, wl.k, QROUTE_SOFTMAX,
+                                 self.logits[r] if logits is None else logits, None, 1, 1.0, self.act, self.limit,
+                                 self.out, self.ids_out, self.wts_out, self.ws, self.ws_bytes, self.status, stream)
+            return
         qexpert_group_act(wl.fmt, self.gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"],
                           wl.E, wl.D, wl.F, x, wl.s, wl.k, ids, wts, self.act, self.limit, self.out, self.ws,
                           self.ws_bytes, self.status, stream)
@@ -314,12 +330,21 @@ class ExpertBench:
         self.x1 = torch.empty_like(self.x[0])
         self.ids1 = torch.empty_like(self.ids[0])
         self.wts1 = torch.empty_like(self.wts[0])
+        if self.device_route:
+            self.logits_pin = torch.from_numpy(self.logits_host.copy()).pin_memory()
+            self.logits1 = torch.empty_like(self.logits[0])
+            return (self.x1.numel() + self.logits1.numel()) * 4, self.out_pin.numel() * 4
         h2d = (self.x1.numel() + self.ids1.numel() + self.wts1.numel()) * 4
         return h2d, self.out_pin.numel() * 4
 
     def e2e_step(self, i, stream):
         r = i % self.nroutes
         self.x1.copy_(self.x_pin[r], non_blocking=True)
+        if self.device_route:
+            self.logits1.copy_(self.logits_pin[r], non_blocking=True)
+            self._call(r, self.x1, None, None, stream, logits=self.logits1)
+            self.out_pin.copy_(self.out, non_blocking=True)
+            return
         self.ids1.copy_(self.ids_pin[r], non_blocking=True)
         self.wts1.copy_(self.wts_pin[r], non_blocking=True)
         self._call(r, self.x1, self.ids1, self.wts1, stream)
@@ -331,6 +356,11 @@ class ExpertBench:
         cfg["l2"] = f"{self.nroutes} seeded routings over the {wl.E * self.expert_bytes / 1e9:.2f} GB store (> L2)"
         cfg["mean_experts_per_step"] = float(np.mean([len(np.unique(r)) for r in self.ids_host]))
         cfg["activation"] = "swiglu" if self.act == 0 else f"swiglu clamped at {self.limit:g}"
+        if self.device_route:
+            cfg["routing"] = "on the device: softmax top-k of seeded N(0,1) router logits, renormalized (qroute)"
+            cfg["mean_experts_per_step"] = float(np.mean(self.route_bytes) / self.expert_bytes)
+        else:
+            cfg["routing"] = "host draws (k distinct experts, softmax of k N(0,1) logits)"
         return cfg
 
 
@@ -473,6 +503,8 @@ def main():
     ap.add_argument("--graph-len", type=int, default=64, help="calls captured per CUDA graph replay")
     ap.add_argument("--sample-seconds", type=float, default=None,
                     help="CPU seconds per oracle sample (reference arm / CPU baseline)")
+    ap.add_argument("--device-route", action="store_true",
+                    help="expert workloads: route on the device from seeded router logits (qexpert_group_routed)")
     ap.add_argument("--swiglu-limit", type=float, default=None,
                     help="expert workloads: clamped SwiGLU with this limit instead of SwiGLU")
     args = ap.parse_args()
@@ -510,7 +542,7 @@ def main():
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024
     bench = (GemvBench(wl, device, l2) if isinstance(wl, synth.GemvWorkload)
-             else ExpertBench(wl, device, args.steps, args.swiglu_limit))
+             else ExpertBench(wl, device, args.steps, args.swiglu_limit, args.device_route))
     stream = torch.cuda.Stream(device)
 
     # warm-up: eager steps, then build the graph (its capture also warms up)

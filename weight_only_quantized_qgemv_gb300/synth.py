@@ -245,6 +245,11 @@ class ExpertWorkload:
     def routing(self, step: int = 0):
         return draw_routing(self.s, self.k, self.E, generator(self.seed, 3, step))
 
+    def router_logits(self, step: int = 0):
+        """Router logits [s][E], N(0, 1), for routing on the device (top-k of them is k
+        experts drawn uniformly without replacement, as in routing())."""
+        return generator(self.seed, 5, step).standard_normal(size=(self.s, self.E), dtype=np.float32)
+
 
 def workload(name: str):
     """The named workload.  Names state format, sizes and batch."""
