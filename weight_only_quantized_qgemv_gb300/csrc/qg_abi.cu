@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "qg_internal.h"
+#include "qg_route.cuh"
 
 namespace qg {
 
@@ -138,9 +139,15 @@ static int rows_per_launch(int fmt, int nm, int I)
 // cost: a row tile of a batch of n pairs costs n (one pass of arithmetic per
 // pair), and CTA c starts at the tile where the cost so far reaches
 // total * c / G.  Tiles stay in order, so results do not change.
-__global__ void __launch_bounds__(1024) k_expert_prep(const int32_t* __restrict__ ids, int P, int k, int E, int smax,
+// With route_kind >= 0 it first routes the tokens itself (one warp per token,
+// route_token), writing ids and wts (which are then outputs) -- the router
+// fused ahead of the expert group, one launch fewer.
+__global__ void __launch_bounds__(1024) k_expert_prep(int32_t* __restrict__ ids, int P, int k, int E, int smax,
                                                       int G, int tpb_up, int tpb_down, unsigned char* ws,
-                                                      WsLayout L, int32_t* status_dev)
+                                                      WsLayout L, int32_t* status_dev, int route_kind,
+                                                      const float* __restrict__ logits,
+                                                      const float* __restrict__ bias, int renorm, float route_scale,
+                                                      float* __restrict__ wts_out)
 {
     __shared__ int s_ids[kMaxPairs + 1];
     __shared__ int s_sorted[kMaxPairs];
@@ -153,10 +160,25 @@ __global__ void __launch_bounds__(1024) k_expert_prep(const int32_t* __restrict_
     int32_t* pair_of = reinterpret_cast<int32_t*>(ws + L.pair_of);
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
-    for (int p = threadIdx.x; p < P; p += blockDim.x) {
-        const int e = ids[p];
-        s_ids[p] = e;
-        if (e < 0 || e >= E) s_bad = 1;
+    if (route_kind >= 0) {
+        const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+        for (int t = threadIdx.x >> 5; t < P / k; t += nw) {
+            int id;
+            float w;
+            route_token<kFusedRouteMaxE / 32>(route_kind, logits + (long long)t * E, bias, E, k, renorm, route_scale,
+                                              lane, id, w);
+            if (lane < k) {
+                s_ids[t * k + lane] = id;
+                ids[t * k + lane] = id;
+                wts_out[t * k + lane] = w;
+            }
+        }
+    } else {
+        for (int p = threadIdx.x; p < P; p += blockDim.x) {
+            const int e = ids[p];
+            s_ids[p] = e;
+            if (e < 0 || e >= E) s_bad = 1;
+        }
     }
     __syncthreads();
     if (s_bad) {
@@ -246,8 +268,9 @@ __global__ void k_expert_combine(const float* __restrict__ wts, int k, int D, co
 cudaError_t expert_prep(const ExpertArgs& a, cudaStream_t st)
 {
     const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
-    return launch_pdl(k_expert_prep, dim3(1), dim3(1024), 0, st, a.ids, a.s * a.k, a.k, a.E, a.smax, a.grid,
-                      a.tpb_up, a.tpb_down, a.ws, L, a.status_dev);
+    return launch_pdl(k_expert_prep, dim3(1), dim3(1024), 0, st, const_cast<int32_t*>(a.ids), a.s * a.k, a.k, a.E,
+                      a.smax, a.grid, a.tpb_up, a.tpb_down, a.ws, L, a.status_dev, a.route_kind, a.logits, a.bias,
+                      a.renorm, a.route_scale, const_cast<float*>(a.wts));
 }
 
 cudaError_t expert_combine(const ExpertArgs& a, cudaStream_t st)
@@ -434,10 +457,36 @@ int qexpert_group(int fmt, int gs, const void* gate, const float* gate_s, const 
                              QACT_SWIGLU, 0.0f, out, workspace, ws_bytes, status_dev, stream);
 }
 
+struct FusedRoute {
+    int kind;
+    const float* logits;
+    const float* bias;
+    int renorm;
+    float scale;
+};
+
+static int expert_group_impl(int fmt, int gs, const void* gate, const float* gate_s, const void* up,
+                             const float* up_s, const void* down, const float* down_s, int E, int D, int F,
+                             const float* x, int s, int k, const int32_t* ids, const float* wts, int act, float limit,
+                             float* out, void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream,
+                             const FusedRoute* route);
+
 int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, const void* up, const float* up_s,
                       const void* down, const float* down_s, int E, int D, int F, const float* x, int s, int k,
                       const int32_t* ids, const float* wts, int act, float limit, float* out, void* workspace,
                       size_t ws_bytes, int32_t* status_dev, void* stream)
+{
+    return expert_group_impl(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, act, limit,
+                             out, workspace, ws_bytes, status_dev, stream, nullptr);
+}
+
+}  // extern "C"
+
+static int expert_group_impl(int fmt, int gs, const void* gate, const float* gate_s, const void* up,
+                             const float* up_s, const void* down, const float* down_s, int E, int D, int F,
+                             const float* x, int s, int k, const int32_t* ids, const float* wts, int act, float limit,
+                             float* out, void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream,
+                             const FusedRoute* route)
 {
     int st = check_act(act, limit);
     if (st) return st;
@@ -483,6 +532,13 @@ int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, co
     a.x = x; a.ids = ids; a.wts = wts; a.out = out;
     a.ws = static_cast<unsigned char*>(workspace);
     a.status_dev = status_dev;
+    if (route) {
+        a.route_kind = route->kind;
+        a.logits = route->logits;
+        a.bias = route->bias;
+        a.renorm = route->renorm;
+        a.route_scale = route->scale;
+    }
     const int up_rows = rows_per_launch(fmt, 2, D), down_rows = rows_per_launch(fmt, 1, F);
     a.smax = up_rows < down_rows ? up_rows : down_rows;
     if (a.smax > kExpertSmax) a.smax = kExpertSmax;
@@ -504,6 +560,8 @@ int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, co
     if (e != cudaSuccess) return launch_status(e);
     return QSTATUS_OK;
 }
+
+extern "C" {
 
 int qroute(int kind, const float* logits, const float* bias, int s, int E, int k, int renorm, float scale,
            int32_t* ids, float* wts, void* stream)
@@ -532,10 +590,23 @@ int qexpert_group_routed(int fmt, int gs, const void* gate, const float* gate_s,
     if ((long long)s * k > kMaxPairs) return QSTATUS_BAD_DIM;
     if (!workspace) return QSTATUS_NULL;
     if (ws_bytes < ws_layout(D, F, s, k).total) return QSTATUS_WORKSPACE;
-    st = qroute(route_kind, logits, bias, s, E, k, renorm, route_scale, ids_out, wts_out, stream);
-    if (st) return st;
-    return qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids_out, wts_out, act,
-                             limit, out, workspace, ws_bytes, status_dev, stream);
+    if (E > kFusedRouteMaxE) {
+        // more experts than the prep kernel's fused routing holds: the router kernel first
+        st = qroute(route_kind, logits, bias, s, E, k, renorm, route_scale, ids_out, wts_out, stream);
+        if (st) return st;
+        return qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids_out, wts_out,
+                                 act, limit, out, workspace, ws_bytes, status_dev, stream);
+    }
+    // the routing inside the expert prep kernel: qroute's checks, then one launch fewer
+    if ((route_kind != QROUTE_SOFTMAX && route_kind != QROUTE_SIGMOID_BIAS) || !(route_scale == route_scale))
+        return QSTATUS_BAD_ROUTE;
+    if (k > E || k > 32) return QSTATUS_BAD_DIM;
+    if (!logits || (route_kind == QROUTE_SIGMOID_BIAS && !bias)) return QSTATUS_NULL;
+    if (!aligned(logits, 4) || (bias && !aligned(bias, 4))) return QSTATUS_MISALIGNED;
+    const FusedRoute fr{route_kind, logits, route_kind == QROUTE_SIGMOID_BIAS ? bias : nullptr, renorm != 0,
+                        route_scale};
+    return expert_group_impl(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids_out, wts_out, act,
+                             limit, out, workspace, ws_bytes, status_dev, stream, &fr);
 }
 
 size_t qgemm_workspace(int I, int s)

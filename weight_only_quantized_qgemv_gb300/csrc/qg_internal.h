@@ -83,7 +83,16 @@ struct ExpertArgs {
     int smax;          // pairs per batch
     int grid;               // CTAs of the streaming launches (<= kMaxGrid)
     int tpb_up, tpb_down;   // row tiles per batch of the tile kernel's two phases
+    // routing fused into the prep kernel (route_kind >= 0, E <= kFusedRouteMaxE):
+    // ids / wts above are then its outputs
+    int route_kind = -1;
+    const float* logits = nullptr;
+    const float* bias = nullptr;
+    int renorm = 0;
+    float route_scale = 1.0f;
 };
+
+constexpr int kFusedRouteMaxE = 256;   // experts the prep kernel's fused routing holds (8 per lane)
 
 // Shared-memory plan of a tile-streaming launch (byte offsets from the start
 // of dynamic shared memory).  The activation rows sit at offset 0, zero-padded

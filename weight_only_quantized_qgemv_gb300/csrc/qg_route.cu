@@ -1,26 +1,12 @@
 // qg_route.cu -- the router on the device: per token, the top k of E experts
-// and their weights from the router logits.
-//
-// colibri keeps this step on the host (docs/vulkan.md, the per-engine host
-// steps: "the router's softmax and top-k"; for the sigmoid routers "sigmoid
-// scores, the correction bias picks, top-k renormalized").  Here one warp per
-// token holds the token's E logits in registers (E/32 per lane, E <= 1024)
-// and runs k rounds of a warp argmax:
-//   softmax:        key = logit (exp is increasing, so the k largest logits
-//                   are the k largest probabilities); weight = softmax
-//                   probability, over all E or renormalized over the k chosen;
-//   sigmoid + bias: key = sigmoid(logit) + bias; weight = sigmoid(logit),
-//                   renormalized over the k chosen if asked;
-// every weight times `scale`.  Ranks run in decreasing key, equal keys lower
-// expert index first; a NaN key ranks below every number.
+// and their weights from the router logits (one warp per token; the routing
+// itself is route_token in qg_route.cuh).
 #include <cuda_runtime.h>
 
 #include "qg_internal.h"
+#include "qg_route.cuh"
 
 namespace qg {
-
-constexpr int kRouteMaxE = 1024;
-constexpr int kRouteMaxK = 32;
 
 __global__ void __launch_bounds__(256) k_route(int kind, const float* __restrict__ logits,
                                                const float* __restrict__ bias, int s, int E, int k, int renorm,
@@ -31,85 +17,12 @@ __global__ void __launch_bounds__(256) k_route(int kind, const float* __restrict
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= s) return;
-    const float* l = logits + (long long)t * E;
-    constexpr int J = kRouteMaxE / 32;
-    float lg[J], key[J];
-    uint32_t taken = 0;                // bit j: expert lane + 32 j chosen
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < J; j++) {
-        const int e = lane + 32 * j;
-        lg[j] = e < E ? l[e] : -INFINITY;
-        float kv = lg[j];
-        if (kind == QROUTE_SIGMOID_BIAS && e < E) kv = 1.0f / (1.0f + expf(-lg[j])) + bias[e];
-        key[j] = (e < E && kv == kv) ? kv : -INFINITY;     // NaN ranks last
-        if (e >= E) taken |= 1u << j;                        // not an expert
-        mx = fmaxf(mx, lg[j]);
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-
-    int my_id = 0;                     // lane r < k: the expert of rank r
-    float my_logit = 0.f;
-    for (int r = 0; r < k; r++) {
-        // this lane's best untaken expert
-        float bk = 0.f;
-        int be = 0x7FFFFFFF;
-#pragma unroll
-        for (int j = 0; j < J; j++) {
-            if (!(taken >> j & 1u) && (be == 0x7FFFFFFF || key[j] > bk)) {
-                bk = key[j];
-                be = lane + 32 * j;
-            }
-        }
-        // the warp's: larger key, then lower index
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, d);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, d);
-            const bool other = oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ok > bk || (ok == bk && oe < be));
-            if (other) {
-                bk = ok;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        // its logit, from the owning lane
-        float vl = 0.f;
-#pragma unroll
-        for (int j = 0; j < J; j++)
-            if (lane + 32 * j == be) vl = lg[j];
-        vl = __shfl_sync(0xffffffffu, vl, be & 31);
-        if (lane == r) {
-            my_id = be;
-            my_logit = vl;
-        }
-    }
-    // weights
-    float wv = 0.f;
-    if (kind == QROUTE_SOFTMAX) {
-        wv = lane < k ? expf(my_logit - mx) : 0.f;
-        float denom = 0.f;
-        if (renorm) {
-            denom = wv;
-        } else {
-#pragma unroll
-            for (int j = 0; j < J; j++)
-                if (lane + 32 * j < E) denom += expf(lg[j] - mx);
-        }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, d);
-        wv = scale * (wv / denom);
-    } else {
-        wv = lane < k ? 1.0f / (1.0f + expf(-my_logit)) : 0.f;
-        float denom = wv;
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, d);
-        wv = scale * (renorm ? wv / denom : wv);
-    }
+    int id;
+    float w;
+    route_token<kRouteMaxE / 32>(kind, logits + (long long)t * E, bias, E, k, renorm, scale, lane, id, w);
     if (lane < k) {
-        ids[(long long)t * k + lane] = my_id;
-        wts[(long long)t * k + lane] = wv;
+        ids[(long long)t * k + lane] = id;
+        wts[(long long)t * k + lane] = w;
     }
 }
 
