@@ -115,3 +115,18 @@ def test_gemm_repeatable():
     a = run_gemm(fmt, gs, w, sc, x, O, I)
     b = run_gemm(fmt, gs, w, sc, x, O, I)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt,gs,O,I,s", [(INT3_G64, 0, 6144, 16384, 64), (MXFP4_E8M0, 0, 2048, 6144, 256),
+                                          (INT8_ROW, 0, 1024, 1024, 300)])
+def test_gemm_workload_shapes_sampled(fmt, gs, O, I, s):
+    """Longer rows and the other workloads' shapes, sampled rows against the oracle."""
+    g = synth.fixed_group(fmt, I, gs or None)
+    rng = synth.generator(199, fmt, O, I, s)
+    w = synth.draw_packed(fmt, O, I, rng)
+    sc = synth.draw_scales(O, I, g, rng, "lognormal", -4.0, fmt=fmt)
+    x = synth.draw_x(s, I, rng)
+    y = run_gemm(fmt, gs, w, sc, x, O, I)
+    rows = sample_rows(O, 40)
+    ystar = oracle.qgemv(fmt, g, packed_rows(fmt, w, O, I, rows), scale_rows(sc, O, rows), x, len(rows), I)
+    assert max_rel(y[:, rows], ystar) <= GATE
