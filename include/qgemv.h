@@ -303,7 +303,7 @@ int qdevice_error(int clear);
 
 /*
  * Kernel choice for the streaming launches of this process (a tuning and
- * testing knob; the surveyed pages have no counterpart).  QKERNEL_AUTO picks
+ * testing knob; the pages have no counterpart).  QKERNEL_AUTO picks
  * per shape; QKERNEL_RING forces the per-lane copy kernel; QKERNEL_TILE the
  * tensor-copy tile kernel wherever its plan fits (else the ring kernel).  Both
  * kernels give the same bits.  Returns the previous policy, or
