@@ -181,3 +181,11 @@ def test_route_checks(L):
     assert L.qexpert_group_routed(*base, 2, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws, None, None) == -10
     assert L.qexpert_group_routed(*base, 0, A, None, 1, 1.0, 5, 0.0, A, A, A, A, ws, None, None) == -9
     assert L.qexpert_group_routed(*base, 0, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws - 1, None, None) == -5
+
+
+def test_empty_sizes_are_rejected(L):
+    """Zero rows, inputs or activation rows: QSTATUS_BAD_DIM before anything is enqueued."""
+    assert L.qgemv(4, 32, A, A, A, 0, 1024, 1, A, None) == -2
+    assert L.qgemv(4, 32, A, A, A, 16, 1024, 0, A, None) == -2
+    assert L.qgemv(1, 0, A, A, A, 16, 0, 1, A, None) == -2
+    assert L.qdequant(4, 32, A, A, 0, 1024, A, None) == -2

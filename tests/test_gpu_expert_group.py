@@ -131,3 +131,16 @@ def test_expert_group_full_size_sampled(name):
     cols = np.unique(np.concatenate([[0, 1, wl.D - 1], synth.generator(5).choice(wl.D, 61, replace=False)]))
     want = oracle_group(wl.fmt, wl.gs, compact_store(wl, used), len(used), wl.D, wl.F, x, cids, wts, cols=cols)
     assert max_rel(out[:, cols], want) <= GATE
+
+
+def test_expert_group_most_pairs():
+    """s * k = 4096 pairs (the limit), every expert routed many times, repeated ids in some rows."""
+    fmt, gs, E, D, F, s, k = INT4_G, 32, 16, 256, 128, 512, 8
+    st = small_store(fmt, E, D, F, 227)
+    rng = synth.generator(229)
+    x = synth.draw_x(s, D, rng)
+    ids = rng.integers(0, E, size=(s, k)).astype(np.int32)
+    wts = rng.random((s, k)).astype(np.float32)
+    out, status = run_group(fmt, gs, st, E, D, F, x, ids, wts)
+    assert status == 0
+    assert max_rel(out, oracle_group(fmt, gs, st, E, D, F, x, ids, wts)) <= GATE

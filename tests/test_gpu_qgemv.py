@@ -117,3 +117,22 @@ def test_qgemv_row_bits_do_not_depend_on_batch(fmt, gs, I):
     for t in range(s):
         y1 = run_gemv(fmt, gs, w, sc, x[t:t + 1], O, I)
         assert np.array_equal(y1[0], ys[t])
+
+
+@pytest.mark.parametrize("fmt,gs,I", [(INT4_G, 32, 36864), (INT3_G64, 0, 43008), (INT8_ROW, 0, 36864),
+                                      (MXFP4_G32, 0, 36864)])
+def test_qgemv_longest_rows(fmt, gs, I):
+    """Rows at the shared-memory staging limit (about 37,000 inputs; int3 43,000), ragged O, s = 1 and 3."""
+    for O, s in [(100, 1), (33, 3)]:
+        g, w, sc, x = inputs(fmt, gs, O, I, s, 211)
+        y = run_gemv(fmt, gs, w, sc, x, O, I)
+        assert max_rel(y, oracle.qgemv(fmt, g, w, sc, x, O, I)) <= GATE
+
+
+def test_qgemv_rows_past_the_limit_are_rejected():
+    from weight_only_quantized_qgemv_gb300 import QStatusError
+    fmt, gs, O, I, s = INT4_G, 32, 8, 40960, 1
+    g, w, sc, x = inputs(fmt, gs, O, I, s, 223)
+    with pytest.raises(QStatusError) as e:
+        run_gemv(fmt, gs, w, sc, x, O, I)
+    assert e.value.status == -2
