@@ -11,8 +11,8 @@
  *                                                     (same section:
  *                                                      coli_vk_expert_group; colibri
  *                                                      docs/vulkan.md, the expert tier:
- *                                                      "every expert's output joins
- *                                                      its row in routing (rank) order")
+ *                                                      each row adds its experts'
+ *                                                      outputs in rank order)
  *   qdequant       the dequantized weights as f32, for checking the decoders
  * The formats are those of the same guide's section "着色器层面的实现细节":
  * int8, int4 decoded nibble - 8 with one f32 scale per group, int3-g64 in two
@@ -248,8 +248,9 @@ int qgemm(int fmt, int gs, const void* w, const float* scales,
  * The router on the device: for each token t < s, the k of E experts with the
  * largest keys and their weights, from the router logits -- the step
  * colibri's engines run on the host (docs/vulkan.md, the per-engine host-step
- * tables: the softmax routers' "softmax and top-k"; the sigmoid routers'
- * scores, correction-bias picks and renormalized top-k).
+ * tables: a softmax followed by a top-k for the softmax routers; sigmoid
+ * scores, a top-k picked with a correction bias and renormalized for the
+ * sigmoid routers).
  *   QROUTE_SOFTMAX       key = logit (the same order as the softmax
  *                        probability); weight = the probability
  *                        exp(l_e) / sum_j exp(l_j) over all E experts, or with

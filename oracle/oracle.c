@@ -12,13 +12,13 @@
  *           "着色器层面的实现细节" (shader-level details: int8, int4 two per
  *           byte decoded nibble-8, int3-g64 one group per 64 inputs in two
  *           planes, one f32 scale per group, MXFP4 e2m1 nibbles with bit 3 the
- *           sign and the scale expanded by the host to f32 per 32 inputs);
+ *           sign, its scale turned into one f32 per 32 inputs on the host);
  *           section "API 契约" (coli_vk_matmul: one quantized GEMV;
  *           coli_vk_gate_up: silu(gate(x))*up(x); coli_vk_expert_group: the
  *           fused MLP of a batch of experts); section "正确性如何在两个实现之间
  *           建立信任" item 3 (int4 is offset binary, nibble - 8).
  *  [VULKAN] colibri "docs/vulkan.md": the expert tier's paragraph on the sum
- *           ("every expert's output joins its row in routing (rank) order"),
+ *           (each row adds its experts' outputs in routing (rank) order),
  *           and the cooperative-matrix paragraph (int8, int4, int3-g64 and
  *           MXFP4 weights decode exactly to fp16, i.e. to small integers and
  *           e2m1 values).
@@ -146,7 +146,7 @@ double oracle_e8m0(int e)
 
 /* The scale of element (o, i): one per group of gs inputs along the row,
  * stored row-major [O][I/gs]: f32, or for MXFP4_E8M0 one ue8m0 byte
- * ([VULKAN] model table: the checkpoints' MXFP4 with ue8m0 scales). */
+ * ([VULKAN] model table: the checkpoints store MXFP4 with ue8m0 scales). */
 static double scale_of(int fmt, const float *scales, long I, long gs, long o, long i)
 {
     gs = group_of(fmt, I, gs);
@@ -214,7 +214,7 @@ double oracle_silu(double z)
  * a limit L (the pages' swiglu_limit, [VULKAN] expert-tier paragraph on
  * GLM-5.3 Flash): the gate is capped at L and the up value clamped to
  * [-L, L] before the product, so that L = 0 zeroes the output (the page's
- * swiglu_clamped "clamps at any limit, including 0"). */
+ * swiglu_clamped clamps at every limit, 0 included). */
 double oracle_glu(int act, double limit, double g, double u)
 {
     if (act == 1) {
@@ -338,9 +338,9 @@ void oracle_expert_group_cols(int fmt, long gs,
 }
 
 /* ------------------------------------------------------------------------
- * The router ([VULKAN] the per-engine host steps: "the router's softmax and
- * top-k" for the softmax models; "sigmoid scores, the correction bias picks,
- * top-k renormalized" for the sigmoid-router models).  Per token t, over its
+ * The router ([VULKAN] the per-engine host steps: a softmax followed by a
+ * top-k for the softmax models; for the sigmoid-router models, sigmoid scores
+ * whose top-k is picked with a correction bias and then renormalized).  Per token t, over its
  * E logits l[t][e]:
  *   kind 0 (softmax): score p_e = exp(l_e) / sum_j exp(l_j); the k largest
  *          p_e are chosen; weight = p_e, or with renorm p_e / sum over the

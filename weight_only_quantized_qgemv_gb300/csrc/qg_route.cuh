@@ -2,8 +2,9 @@
 // expert prep kernel's fused routing).
 //
 // colibri keeps this step on the host (docs/vulkan.md, the per-engine host
-// steps: "the router's softmax and top-k"; for the sigmoid routers "sigmoid
-// scores, the correction bias picks, top-k renormalized").  The warp holds
+// steps: a softmax followed by a top-k for most models; for the sigmoid
+// routers, sigmoid scores whose top-k is picked with a correction bias and
+// then renormalized).  The warp holds
 // the token's E logits in registers (J per lane, E <= 32 J) and runs k rounds
 // of a warp argmax:
 //   softmax:        key = logit (exp is increasing, so the k largest logits
