@@ -299,7 +299,7 @@ class ExpertBench:
             self.wts_out = torch.empty(wl.s, wl.k, dtype=torch.float32, device=device)
             top = np.argpartition(-self.logits_host, wl.k - 1, axis=2)[:, :, :wl.k]
             self.route_bytes = [len(np.unique(top[r])) * self.expert_bytes for r in range(self.nroutes)]
-            self.launches_per_step = 5
+            self.launches_per_step = 4 if wl.E <= 256 else 5   # routing fused into the prep kernel up to 256 experts
 
     def _call(self, r, x, ids, wts, stream, logits=None):
         from weight_only_quantized_qgemv_gb300 import QROUTE_SOFTMAX, qexpert_group_act, qexpert_group_routed
