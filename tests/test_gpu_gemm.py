@@ -130,3 +130,27 @@ def test_gemm_workload_shapes_sampled(fmt, gs, O, I, s):
     rows = sample_rows(O, 40)
     ystar = oracle.qgemv(fmt, g, packed_rows(fmt, w, O, I, rows), scale_rows(sc, O, rows), x, len(rows), I)
     assert max_rel(y[:, rows], ystar) <= GATE
+
+
+@pytest.mark.parametrize("fmt,gs", [(INT4_G, 32), (INT3_G64, 0)])
+def test_gemm_longest_rows(fmt, gs):
+    """The longest rows qgemm takes (2^20 inputs): 16384 steps along K in one CTA.
+
+    At this length the worst-case f32 bound is looser than the gate itself,
+    so the gate alone is checked."""
+    O, I, s = 130, 1 << 20, 3
+    g, w, sc, x = inputs(fmt, gs, O, I, s, 223)
+    y = run_gemm(fmt, gs, w, sc, x, O, I)
+    ystar = oracle.qgemv(fmt, g, w, sc, x, O, I)
+    assert np.isfinite(y).all()
+    assert max_rel(y, ystar) <= GATE
+
+
+def test_gemm_most_activation_rows():
+    """The most activation rows qgemm takes (65536): 512 column tiles of 128 rows."""
+    fmt, gs, O, I, s = INT4_G, 32, 96, 128, 1 << 16
+    g, w, sc, x = inputs(fmt, gs, O, I, s, 227)
+    y = run_gemm(fmt, gs, w, sc, x, O, I)
+    ystar = oracle.qgemv(fmt, g, w, sc, x, O, I)
+    assert max_rel(y, ystar) <= GATE
+    assert np.all(np.abs(y - ystar) <= f32_bound(fmt, g, w, sc, x, O, I))

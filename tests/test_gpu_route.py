@@ -74,11 +74,29 @@ def test_route_ties_and_nan():
     assert ids[0].tolist() == [10, 20, 0]
 
 
+@pytest.mark.parametrize("kind", [QROUTE_SOFTMAX, QROUTE_SIGMOID_BIAS])
+@pytest.mark.parametrize("s,k", [(1, 32), (65, 32)])
+def test_route_largest_sizes(kind, s, k):
+    """The most experts (1024) and the most choices per token (32) a call takes."""
+    E = 1024
+    rng = synth.generator(211, kind, s, k)
+    logits = (2 * rng.standard_normal((s, E))).astype(np.float32)
+    bias = (0.2 * rng.standard_normal(E)).astype(np.float32) if kind == QROUTE_SIGMOID_BIAS else None
+    ids, w = run_route(kind, logits, bias, k, 1, 1.0)
+    want_ids, want_w = oracle.route(kind, logits, bias, k=k, renorm=True)
+    assert np.array_equal(ids, want_ids)
+    assert np.abs(w - want_w).max() <= 1e-6 * np.abs(want_w).max()
+
+
 @pytest.mark.parametrize("fmt,gs", [(MXFP4_G32, 0), (INT4_G, 32)])
 @pytest.mark.parametrize("kind", [QROUTE_SOFTMAX, QROUTE_SIGMOID_BIAS])
-def test_expert_group_routed(fmt, gs, kind):
-    """Routing and the expert group in one call: the two calls' bits, and the oracle's result."""
-    E, D, F, s, k = 16, 256, 128, 5, 4
+@pytest.mark.parametrize("E", [16, 256, 300])
+def test_expert_group_routed(fmt, gs, kind, E):
+    """Routing and the expert group in one call: the two calls' bits, and the oracle's result.
+
+    Up to 256 experts the routing runs inside the expert group's first kernel;
+    past that it is a router launch of its own ahead of it (E = 300)."""
+    D, F, s, k = 256, 128, 5, 4
     st = small_store(fmt, E, D, F, 193)
     rng = synth.generator(197, fmt, kind)
     x = synth.draw_x(s, D, rng)
