@@ -14,6 +14,14 @@
  *                                                      each row adds its experts'
  *                                                      outputs in rank order)
  *   qdequant       the dequantized weights as f32, for checking the decoders
+ *   qgemm          the same product as qgemv for many activation rows, on the
+ *                  tensor cores (prefill)   (colibri docs/vulkan.md, the
+ *                                            tiled-GEMM / cooperative-matrix
+ *                                            paragraph)
+ *   qroute         the router's top-k and weights on the device, and
+ *   qexpert_group_routed  the router chained ahead of the expert group
+ *                                           (docs/vulkan.md, the per-engine
+ *                                            host-step tables)
  * The formats are those of the same guide's section "着色器层面的实现细节":
  * int8, int4 decoded nibble - 8 with one f32 scale per group, int3-g64 in two
  * bit planes with one f32 scale per 64 inputs, and MXFP4 (e2m1 nibbles, bit 3
@@ -22,7 +30,7 @@
  * Conventions for every call:
  *  - All array pointers are DEVICE pointers, owned by the caller.  The library
  *    allocates no device memory and keeps no state between calls; scratch
- *    that a call needs (qexpert_group) is a caller-provided workspace.
+ *    that a call needs (qexpert_group, qgemm) is a caller-provided workspace.
  *  - Calls are asynchronous on the given CUDA stream (`stream` is a
  *    cudaStream_t; NULL is the legacy default stream).  They return once the
  *    work is enqueued; the caller synchronizes before reading results.
@@ -55,9 +63,9 @@
  *                      stored: `scales` points to uint8 ue8m0 bytes [O][I/32]
  *                      (value 2^(e - 127); e = 255 is NaN), read in place of
  *                      the host-expanded f32; gs must be 0 or 32.
- *  - Alignment: packed weights and activation/hidden vectors (x, h, workspace)
- *    16-byte aligned; scales and outputs 4-byte aligned (ue8m0 scale bytes
- *    too); else QSTATUS_MISALIGNED.
+ *  - Alignment: packed weights and activation/hidden vectors (x, h) 16-byte
+ *    aligned; workspaces 256-byte aligned; scales and outputs 4-byte aligned
+ *    (ue8m0 scale bytes too); else QSTATUS_MISALIGNED.
  *  - Sizes: I % 16 == 0 (int8), I % 32 == 0 (int4 per row), I % 128 == 0
  *    (MXFP4 with ue8m0 bytes), I % gs == 0 (grouped formats), O, I, s >= 1.
  *    The activation rows of one launch share shared memory with the weight
@@ -93,7 +101,7 @@ enum {
     QSTATUS_BAD_DIM = -2,        /* a size out of range or not a multiple it must be */
     QSTATUS_MISALIGNED = -3,     /* a pointer without the alignment stated above */
     QSTATUS_NULL = -4,           /* a required pointer is NULL */
-    QSTATUS_WORKSPACE = -5,      /* workspace smaller than qexpert_group_workspace() */
+    QSTATUS_WORKSPACE = -5,      /* workspace smaller than the call's *_workspace() size */
     QSTATUS_LAUNCH = -6,         /* CUDA reported an error at launch */
     QSTATUS_DEVICE_TIMEOUT = -7, /* a bounded device-side wait ran out */
     QSTATUS_BAD_EXPERT_ID = -8,  /* an expert id outside [0, E) (reported on the device) */
@@ -154,7 +162,7 @@ size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
  *   x         f32 [s][D];  ids int32 [s][k];  wts f32 [s][k]
  *   out       f32 [s][D], written
  *   workspace device scratch of ws_bytes >= qexpert_group_workspace(E, D, F, s, k)
- *             bytes; its contents on entry do not matter.
+ *             bytes, 256-byte aligned; its contents on entry do not matter.
  *   status_dev optional device int32: set to QSTATUS_OK, or to
  *             QSTATUS_BAD_EXPERT_ID when an id is outside [0, E) -- then out is
  *             all zeros.  The host-side return cannot see device-side checks.
@@ -237,7 +245,10 @@ int qdequant(int fmt, int gs, const void* w, const float* scales,
  *   s) device bytes, 256-byte aligned, contents on entry irrelevant.
  * Every format, with I % 64 == 0 and groups of at least 32 inputs
  * (QFMT_INT8_G with gs 16: QSTATUS_BAD_FMT).  Intended for s >= 16; any s >= 1
- * works.  I <= 2^20, s <= 65536.
+ * works.  I <= 2^20, s <= 65536; O, I or s below 1 or past these limits, or I
+ * not a multiple of 64: QSTATUS_BAD_DIM.  A workspace smaller than
+ * qgemm_workspace(I, s): QSTATUS_WORKSPACE; one not 256-byte aligned:
+ * QSTATUS_MISALIGNED.  qgemm_workspace returns 0 for I or s below 1.
  */
 size_t qgemm_workspace(int I, int s);
 int qgemm(int fmt, int gs, const void* w, const float* scales,
@@ -262,8 +273,10 @@ int qgemm(int fmt, int gs, const void* w, const float* scales,
  * NaN key ranks below every number.
  *   logits f32 [s][E];  bias f32 [E] (QROUTE_SIGMOID_BIAS only, else may be
  *   NULL);  ids int32 [s][k] and wts f32 [s][k], written in rank order.
- * 1 <= k <= 32, k <= E <= 1024.  QSTATUS_BAD_ROUTE for an unknown kind or a
- * NaN scale.
+ * s >= 1, 1 <= k <= 32, k <= E <= 1024, else QSTATUS_BAD_DIM.
+ * QSTATUS_BAD_ROUTE for an unknown kind or a NaN scale; QSTATUS_NULL for a
+ * missing logits, ids or wts pointer, or a missing bias with
+ * QROUTE_SIGMOID_BIAS; QSTATUS_MISALIGNED for a pointer not 4-byte aligned.
  */
 #define QROUTE_SOFTMAX 0
 #define QROUTE_SIGMOID_BIAS 1

@@ -156,6 +156,10 @@ def test_qgemm_checks(L):
     assert L.qgemm(4, 32, A, A, A, 16, 6144, 512, A, None, ws, None) == -4   # no workspace
     assert L.qgemm(4, 32, A, A, A, 16, 6144, 512, A, A + 16, ws, None) == -3  # workspace not 256-aligned
     assert L.qgemm(4, 32, A, A, A, 16, 6144, 0, A, A, ws, None) == -2       # s < 1
+    assert L.qgemm(4, 32, A, A, A, 0, 6144, 512, A, A, ws, None) == -2      # O < 1
+    big = L.qgemm_workspace((1 << 20) + 64, 1 << 17)
+    assert L.qgemm(4, 32, A, A, A, 16, (1 << 20) + 64, 8, A, A, big, None) == -2   # I past 2^20
+    assert L.qgemm(4, 32, A, A, A, 16, 64, (1 << 16) + 1, A, A, big, None) == -2   # s past 65536
 
 
 def test_route_checks(L):

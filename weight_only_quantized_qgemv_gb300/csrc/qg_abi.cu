@@ -345,9 +345,9 @@ const char* qstatus_string(int status)
     case QSTATUS_BAD_FMT: return "unknown weight format, or a group size that format does not allow";
     case QSTATUS_BAD_DIM: return "a size is out of range or not the multiple its format needs";
     case QSTATUS_MISALIGNED: return "a pointer lacks the required alignment (16 B for packed weights and "
-                                    "activations, 4 B for scales and outputs)";
+                                    "activations, 256 B for workspaces, 4 B for scales and outputs)";
     case QSTATUS_NULL: return "a required pointer is NULL";
-    case QSTATUS_WORKSPACE: return "workspace smaller than qexpert_group_workspace()";
+    case QSTATUS_WORKSPACE: return "workspace smaller than the call's *_workspace() size";
     case QSTATUS_LAUNCH: return "CUDA reported an error at launch (see qlast_cuda_error)";
     case QSTATUS_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case QSTATUS_BAD_EXPERT_ID: return "an expert id is outside [0, E)";
