@@ -193,3 +193,26 @@ def test_empty_sizes_are_rejected(L):
     assert L.qgemv(4, 32, A, A, A, 16, 1024, 0, A, None) == -2
     assert L.qgemv(1, 0, A, A, A, 16, 0, 1, A, None) == -2
     assert L.qdequant(4, 32, A, A, 0, 1024, A, None) == -2
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """The binding passes device addresses only: a host tensor or a strided
+    view is refused before the library is called."""
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _lib._ptr(torch.zeros(4))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _lib._ptr(object())
+    assert _lib._ptr(None) is None
+    assert _lib._ptr(4096) == 4096
+
+    class View:                         # a CUDA tensor's interface, strided
+        is_cuda = True
+
+        def is_contiguous(self):
+            return False
+
+        def data_ptr(self):
+            raise AssertionError("must not be reached")
+    with pytest.raises(ValueError, match="contiguous"):
+        _lib._ptr(View())

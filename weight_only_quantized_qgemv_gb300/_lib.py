@@ -94,10 +94,17 @@ def lib() -> ctypes.CDLL:
 
 
 def _ptr(a):
+    """The device address of an array argument.  A tensor must live on a CUDA
+    device and be contiguous (the library reads dense row-major arrays); a
+    host tensor or a strided view is refused here, before any launch."""
     if a is None:
         return None
     if isinstance(a, int):
         return a
+    if not getattr(a, "is_cuda", False):
+        raise ValueError(f"expected a CUDA tensor, got one on {getattr(a, 'device', type(a).__name__)}")
+    if not a.is_contiguous():
+        raise ValueError("expected a contiguous tensor (dense row-major layout)")
     return a.data_ptr()
 
 
