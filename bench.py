@@ -410,10 +410,9 @@ def oracle_sample_runner(wl, target_s: float, swiglu_limit=None):
             f"{nrows} gate/up rows (cycling over the {wl.F} rows) of expert {int(ids[0, 0])} (token 0, first routing)")
 
 
-def cpu_baseline(wl, target_s=12.0, swiglu_limit=None):
-    """The oracle on the host cores: samples of about a second, repeated until
-    about target_s seconds of CPU work."""
-    from oracle import oracle as orc
+def _time_oracle(wl, target_s, swiglu_limit):
+    """GB/s of the oracle over samples of about a second, repeated until about
+    target_s seconds of CPU work, and a description of the sample."""
     run, desc = oracle_sample_runner(wl, min(1.0, target_s), swiglu_limit)
     t = time.perf_counter()
     nbytes, n = 0, 0
@@ -423,8 +422,24 @@ def cpu_baseline(wl, target_s=12.0, swiglu_limit=None):
         dt = time.perf_counter() - t
         if dt >= target_s:
             break
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": orc.threads(), "kind": "oracle",
-            "sample": f"{n} samples of {desc}; {dt:.1f} s"}
+    return nbytes / dt / 1e9, f"{n} samples of {desc}; {dt:.1f} s"
+
+
+def cpu_baseline(wl, target_s=12.0, swiglu_limit=None):
+    """The oracle on all the host cores (OpenMP over output rows), and on one
+    core for about half as long."""
+    from oracle import oracle as orc
+    cores = orc.threads()
+    value, sample = _time_oracle(wl, target_s, swiglu_limit)
+    out = {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if cores > 1:
+        orc.set_threads(1)
+        try:
+            v1, sample1 = _time_oracle(wl, target_s / 2, swiglu_limit)
+        finally:
+            orc.set_threads(cores)
+        out["single_core"] = {"value": v1, "unit": "GB/s", "cores": 1, "sample": sample1}
+    return out
 
 
 def reference_arm(args, wl, world, rank):
@@ -451,6 +466,45 @@ def reference_arm(args, wl, world, rank):
                              "sample": desc + " per step"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def percentiles(us):
+    a = np.asarray(us, dtype=np.float64)
+    return {"p10": float(np.percentile(a, 10)), "p50": float(np.percentile(a, 50)),
+            "p90": float(np.percentile(a, 90))}
+
+
+def call_distribution(bench, graphs, G, per_call_s, stream, torch, n_replays=50, n_eager=200):
+    """µs per call as a distribution (not part of the timed region): per-replay
+    events over the CUDA graphs (each replay = G back-to-back calls), and
+    n_eager single calls each between its own pair of events.  The eager calls
+    are enqueued behind tens of milliseconds of graph replays, so the device
+    never waits on the host between them; an event between two calls also
+    keeps one call from starting early under the previous one."""
+    ng = len(graphs)
+    reps = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_replays)]
+    # enough queued device work to cover the host's enqueueing of the eager
+    # calls (tens of µs each from Python) with room to spare
+    lead = max(1, int(-(-(20e-3 + 60e-6 * n_eager) // max(per_call_s * G, 1e-9))))
+    calls = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_eager)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for r, (a, b) in enumerate(reps):
+            a.record(stream)
+            graphs[r % ng].replay()
+            b.record(stream)
+        for r in range(lead):
+            graphs[r % ng].replay()
+        for i, (a, b) in enumerate(calls):
+            a.record(stream)
+            bench.step(i, stream.cuda_stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    graph_us = [a.elapsed_time(b) * 1e3 / G for a, b in reps]
+    eager_us = [a.elapsed_time(b) * 1e3 for a, b in calls]
+    return {"graph": {"replays": n_replays, "calls_per_replay": G, "us_per_call": percentiles(graph_us)},
+            "eager": {"calls": n_eager, "us_per_call": percentiles(eager_us),
+                      "note": "each call alone between two events, behind queued work"}}
 
 
 def gemv_kernel_name(wl, sms=152):
@@ -588,6 +642,8 @@ def main():
     achieved = (nbytes / steps_done) / per_launch_s / 1e9
     peak, peak_src = hbm_peak()
 
+    timing = call_distribution(bench, graphs, G, per_launch_s, stream, torch)
+
     # end to end through the public API, host buffers, copies inside the timed region
     h2d, d2h = bench.e2e_setup()
     k_e2e = min(args.steps, 2000)
@@ -636,6 +692,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": t_max / steps_done * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "us_per_call": per_launch_s * 1e6,
+        "timing": timing,
         "roofline": roof,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

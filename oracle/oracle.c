@@ -412,3 +412,16 @@ int oracle_threads(void)
     return 1;
 #endif
 }
+
+/* Sets the number of threads the OpenMP loops use (n >= 1; ignored when built
+ * without OpenMP).  Only the timing of the oracle depends on it: each output
+ * row is computed by one thread in the same order whatever the count. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

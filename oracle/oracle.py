@@ -98,10 +98,17 @@ class Oracle:
         lib.oracle_sigmoid.restype = D
         lib.oracle_route.argtypes = [I, P, P, L, L, L, I, D, P, P, P, P]
         lib.oracle_threads.restype = I
+        lib.oracle_set_threads.argtypes = [I]
+        lib.oracle_set_threads.restype = None
         self.lib = lib
 
     def threads(self) -> int:
         return self.lib.oracle_threads()
+
+    def set_threads(self, n: int) -> None:
+        """Threads of the OpenMP loops from here on (timing only: every output
+        row is one thread's index-order sum whatever the count)."""
+        self.lib.oracle_set_threads(int(n))
 
     def packed_bytes(self, fmt: int, O: int, I: int) -> int:
         return self.lib.oracle_packed_bytes(fmt, O, I)
@@ -229,7 +236,7 @@ def default() -> Oracle:
 
 def __getattr__(name):
     # Module-level access to the default copy's methods: oracle.qgemv(...), ...
-    if name in {"threads", "packed_bytes", "codes", "e2m1", "code_value", "e8m0", "silu", "glu", "dequant_f32",
+    if name in {"threads", "set_threads", "packed_bytes", "codes", "e2m1", "code_value", "e8m0", "silu", "glu", "dequant_f32",
                 "qgemv", "qgemv_rows", "qgate_up", "qgate_up_rows", "expert_group", "sigmoid", "route"}:
         return getattr(default(), name)
     raise AttributeError(name)

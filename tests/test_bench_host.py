@@ -63,3 +63,25 @@ def test_reference_arm_two_ranks_prints_once():
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_percentiles():
+    sys.path.insert(0, ROOT)
+    import bench
+    p = bench.percentiles(list(range(1, 102)))          # 1 .. 101
+    assert p == {"p10": 11.0, "p50": 51.0, "p90": 91.0}
+
+
+def test_cpu_baseline_all_cores_and_one():
+    """The oracle timed on all host cores and on one; the thread count is restored."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import oracle
+    from weight_only_quantized_qgemv_gb300 import synth
+    cores = oracle.threads()
+    cpu = bench.cpu_baseline(synth.workload("int8_row_1024x1024_s1"), target_s=0.4)
+    assert cpu["kind"] == "oracle" and cpu["unit"] == "GB/s" and cpu["value"] > 0
+    assert cpu["cores"] == cores
+    if cores > 1:
+        assert cpu["single_core"]["cores"] == 1 and cpu["single_core"]["value"] > 0
+    assert oracle.threads() == cores
