@@ -216,3 +216,64 @@ def test_binding_refuses_host_and_strided_tensors():
             raise AssertionError("must not be reached")
     with pytest.raises(ValueError, match="contiguous"):
         _lib._ptr(View())
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "qgemv.h"
+
+static int fails = 0;
+#define EXPECT(cond) do { if (!(cond)) { printf("FAIL %s\n", #cond); fails++; } } while (0)
+
+int main(void)
+{
+    int st;
+    for (st = 0; st >= -10; st--) printf("%d %s\n", st, qstatus_string(st));
+    EXPECT(strcmp(qstatus_string(12345), "unknown status") == 0);
+    EXPECT(qgemm_workspace(6144, 512) > 0 && qgemm_workspace(0, 4) == 0);
+    EXPECT(qexpert_group_workspace(256, 6144, 2048, 8, 8) > 0);
+    /* host-side checks only: nothing reaches a device */
+    EXPECT(qgemv(3, 0, NULL, NULL, NULL, 16, 1024, 1, NULL, NULL) == QSTATUS_BAD_FMT);
+    EXPECT(qgemv(QFMT_INT4_G, 32, NULL, NULL, NULL, 16, 1024, 0, NULL, NULL) == QSTATUS_BAD_DIM);
+    EXPECT(qgemv(QFMT_INT4_G, 32, NULL, NULL, NULL, 16, 1024, 1, NULL, NULL) == QSTATUS_NULL);
+    EXPECT(qgemm(QFMT_INT3_G64, 0, NULL, NULL, NULL, 16, 1000, 4, NULL, NULL, 0, NULL) == QSTATUS_BAD_DIM);
+    EXPECT(qroute(2, NULL, NULL, 1, 8, 2, 1, 1.0f, NULL, NULL, NULL) == QSTATUS_BAD_ROUTE);
+    EXPECT(qgate_up_act(QFMT_MXFP4_G32, 0, NULL, NULL, NULL, NULL, NULL, 16, 64, 1, 7, 0.0f, NULL, NULL)
+           == QSTATUS_BAD_ACT);
+    EXPECT(qkernel_policy(99) == QSTATUS_BAD_FMT);
+    EXPECT(qkernel_policy(QKERNEL_AUTO) == QKERNEL_AUTO);
+    printf("fails %d\n", fails);
+    return fails != 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_cpp_and_links(L, tmp_path):
+    """A plain C99 program, built with -Wall -Wextra -pedantic -Werror against
+    include/qgemv.h and linked to the library, calls the entry points that need
+    no GPU; the header also compiles as C++ (its extern "C" guard)."""
+    import shutil
+    import subprocess
+    gcc, gxx = shutil.which("gcc"), shutil.which("g++")
+    if not gcc or not gxx:
+        pytest.skip("no host C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    libdir = os.path.dirname(_build.LIB)
+    exe = tmp_path / "client"
+    inc = os.path.join(ROOT, "include")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src), "-o", str(exe),
+                    "-L", libdir, "-l:" + os.path.basename(_build.LIB), "-Wl,-rpath," + libdir],
+                   check=True, capture_output=True, text=True)
+    cpp = tmp_path / "client.cpp"
+    cpp.write_text('#include "qgemv.h"\nint main() { return qgemm_workspace(0, 0) != 0; }\n')
+    subprocess.run([gxx, "-std=c++17", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", inc,
+                    str(cpp)], check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = r.stdout.splitlines()
+    assert lines[-1] == "fails 0"
+    for line in lines[:11]:
+        st, text = line.split(" ", 1)
+        assert text == L.qstatus_string(int(st)).decode()
