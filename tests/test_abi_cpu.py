@@ -277,3 +277,86 @@ def test_header_compiles_as_c_and_cpp_and_links(L, tmp_path):
     for line in lines[:11]:
         st, text = line.split(" ", 1)
         assert text == L.qstatus_string(int(st)).decode()
+
+
+# The header's rules for format, group size and sizes, restated per format:
+# (allowed gs values as a predicate of (gs, I), the multiple I must be).
+_POW2 = lambda g, lo, hi: lo <= g <= hi and g & (g - 1) == 0
+HEADER_RULES = {
+    1: (lambda g, I: g in (0, I), lambda g: 16),                     # int8 per row
+    2: (lambda g, I: g in (0, I), lambda g: 32),                     # int4 per row
+    4: (lambda g, I: _POW2(g, 32, 1024), lambda g: g),               # int4 grouped
+    5: (lambda g, I: g in (0, 64), lambda g: 64),                    # int3-g64
+    7: (lambda g, I: g in (0, 32), lambda g: 32),                    # MXFP4, f32 scales
+    8: (lambda g, I: g in (0, 32), lambda g: 128),                   # MXFP4, ue8m0 bytes
+    13: (lambda g, I: _POW2(g, 16, 512), lambda g: g),               # int8 grouped
+}
+
+
+def expected_statuses(fmt, gs, I, dims_ok, gemm=False):
+    """Every status the header allows for these arguments (NULL pointers):
+    the statuses of all violated rules, or QSTATUS_NULL if none is violated."""
+    bad = set()
+    rule = HEADER_RULES.get(fmt)
+    if rule is None or not rule[0](gs, I):
+        bad.add(-1)
+    else:
+        if I % rule[1](gs):
+            bad.add(-2)
+        if gemm and (I if fmt in (1, 2) else {5: 64, 7: 32, 8: 32}.get(fmt, gs)) < 32:
+            bad.add(-1)                                               # qgemm: groups of >= 32 inputs
+    if not dims_ok:
+        bad.add(-2)
+    return bad or {-4}
+
+
+def _draw_case(rng, i_max):
+    fmt = int(rng.choice([1, 2, 4, 5, 7, 8, 13])) if rng.random() < 0.8 else int(rng.choice([0, 3, 6, -1, 99]))
+    base = int(rng.choice([16, 32, 64, 128, 256, 1024]))
+    I = int(rng.choice([base * int(rng.integers(1, max(2, i_max // base))), int(rng.integers(-64, 40000)), 0,
+                        i_max, i_max + 64], p=[0.6, 0.25, 0.05, 0.05, 0.05]))
+    likely = {1: [0, I], 2: [0, I], 4: [32, 64, 128, 256, 512, 1024], 5: [0, 64], 7: [0, 32], 8: [0, 32],
+              13: [16, 32, 64, 128, 256, 512]}.get(fmt, [0])
+    gs = int(rng.choice(likely)) if rng.random() < 0.6 else \
+        int(rng.choice([0, 8, 16, 32, 48, 64, 128, 256, 512, 1024, 2048, I]))
+    O = int(rng.choice([-1, 0, 1, int(rng.integers(1, 100000))]))
+    s = int(rng.choice([-1, 0, 1, 8, 9, int(rng.integers(1, 70000))]))
+    return fmt, gs, I, O, s
+
+
+def test_size_checks_follow_the_header_rules(L):
+    """qgemv, qdequant and qgemm on random formats, group sizes and sizes, all
+    with NULL pointers (nothing reaches a device): the status is one the
+    header's rules give for the violated rule, or QSTATUS_NULL when every size
+    rule holds."""
+    import numpy as np
+    from collections import Counter
+    seen = {"qgemv": Counter(), "qdequant": Counter(), "qgemm": Counter()}
+    rng = np.random.default_rng(2024)
+    Z = ctypes.c_size_t
+    L.qgemm.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + \
+        [ctypes.c_void_p, ctypes.c_void_p, Z, ctypes.c_void_p]
+    for _ in range(3000):
+        fmt, gs, I, O, s = _draw_case(rng, 36864)
+        want = expected_statuses(fmt, gs, I, O >= 1 and 1 <= I <= 36864 and s >= 1)
+        if 36864 < I <= 51200 and want == {-2}:
+            # rows the header gives only as "about 37,000" at most: the
+            # shared-memory budget is checked with the launch shape, after
+            # the pointers
+            want = {-2, -4}
+        got = L.qgemv(fmt, gs, None, None, None, O, I, s, None, None)
+        assert got in want, (fmt, gs, I, O, s, got, want)
+        seen["qgemv"][got] += 1
+        want = expected_statuses(fmt, gs, I, O >= 1 and I >= 1)
+        got = L.qdequant(fmt, gs, None, None, O, I, None, None)
+        assert got in want, ("qdequant", fmt, gs, I, O, got, want)
+        seen["qdequant"][got] += 1
+    for _ in range(3000):
+        fmt, gs, I, O, s = _draw_case(rng, 1 << 20)
+        dims_ok = O >= 1 and 1 <= I <= (1 << 20) and I % 64 == 0 and 1 <= s <= (1 << 16)
+        want = expected_statuses(fmt, gs, I, dims_ok, gemm=True)
+        got = L.qgemm(fmt, gs, None, None, None, O, I, s, None, None, 0, None)
+        assert got in want, ("qgemm", fmt, gs, I, O, s, got, want)
+        seen["qgemm"][got] += 1
+    for name, c in seen.items():           # every outcome is reached often
+        assert min(c[-1], c[-2], c[-4]) >= 100, (name, dict(c))
