@@ -360,3 +360,45 @@ def test_size_checks_follow_the_header_rules(L):
         seen["qgemm"][got] += 1
     for name, c in seen.items():           # every outcome is reached often
         assert min(c[-1], c[-2], c[-4]) >= 100, (name, dict(c))
+
+
+def test_expert_group_checks_follow_the_header_rules(L):
+    """qexpert_group_act on random formats, group sizes, sizes, pair counts and
+    activations, all with NULL pointers: the status is one the header's rules
+    give for a violated rule (gs applies to the D-long gate/up rows and the
+    F-long down rows alike; s * k <= 4096), or QSTATUS_NULL."""
+    import math
+    from collections import Counter
+
+    import numpy as np
+    rng = np.random.default_rng(2025)
+    f = ctypes.c_float
+    L.qexpert_group_act.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 6 + [ctypes.c_int] * 3 + \
+        [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, f,
+         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+    seen = Counter()
+    for _ in range(4000):
+        fmt, gs, D, _, s = _draw_case(rng, 36864)
+        F = int(rng.choice([D, 2048, 128, 96, 40000, 0], p=[0.5, 0.2, 0.1, 0.1, 0.05, 0.05]))
+        E = int(rng.choice([0, 1, 256, -3], p=[0.05, 0.2, 0.7, 0.05]))
+        k = int(rng.choice([0, 1, 8, 32, 600], p=[0.05, 0.3, 0.4, 0.15, 0.1]))
+        act = int(rng.choice([0, 1, 2, -1], p=[0.45, 0.45, 0.05, 0.05]))
+        limit = float(rng.choice([0.0, 7.0, -1.0, math.inf, math.nan], p=[0.25, 0.45, 0.1, 0.1, 0.1]))
+        want = set()
+        if act not in (0, 1) or (act == 1 and not limit >= 0):
+            want.add(-9)
+        for n in (D, F):               # every violated rule of either row length
+            if fmt not in HEADER_RULES or not HEADER_RULES[fmt][0](gs, n):
+                want.add(-1)
+            elif n % HEADER_RULES[fmt][1](gs):
+                want.add(-2)
+        if min(E, D, F, s, k) < 1 or max(D, F) > 51200 or s * k > 4096:
+            want.add(-2)
+        if not want and max(D, F) > 36864:
+            want = {-2, -4}            # the shared-memory budget, checked with the launch shape
+        want = want or {-4}
+        got = L.qexpert_group_act(fmt, gs, None, None, None, None, None, None, E, D, F, None, s, k, None, None,
+                                  act, limit, None, None, 0, None, None)
+        assert got in want, (fmt, gs, E, D, F, s, k, act, limit, got, want)
+        seen[got] += 1
+    assert min(seen[-1], seen[-2], seen[-4], seen[-9]) >= 100, dict(seen)
