@@ -109,3 +109,34 @@ def test_expert_group_clamped(fmt, gs, E, s, k):
     inf, _ = run_group_act(fmt, gs, st, E, D, F, x, ids, wts, QACT_SWIGLU_CLAMPED, float("inf"))
     plain, _ = run_group_act(fmt, gs, st, E, D, F, x, ids, wts, QACT_SWIGLU, 0.0)
     assert np.array_equal(inf.view(np.uint32), plain.view(np.uint32))
+
+
+def test_expert_group_clamped_full_size_sampled():
+    """The clamped-SwiGLU configuration the bench times: the MXFP4 expert
+    workload (256 experts, D = 6144, F = 2048, top 8) with limit 7, sampled
+    output columns against the oracle."""
+    from test_gpu_expert_group import compact_store, full_store_on_device
+    wl = synth.workload("mxfp4_experts_E256_D6144_F2048_s1_k8")
+    L = 7.0
+    d = full_store_on_device(wl)
+    x = wl.x()
+    ids, wts = wl.routing()
+    ws_bytes = qexpert_group_workspace(wl.E, wl.D, wl.F, wl.s, wl.k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
+    out = empty_f32(wl.s, wl.D)
+    qexpert_group_act(wl.fmt, 0, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], wl.E, wl.D,
+                      wl.F, dev(x), wl.s, wl.k, dev(ids.astype(np.int32)), dev(wts.astype(np.float32)),
+                      QACT_SWIGLU_CLAMPED, L, out, ws, ws_bytes, status)
+    assert int(host(status)[0]) == 0
+    y = host(out)
+    assert np.isfinite(y).all()
+    used = np.unique(ids)
+    remap = {int(e): i for i, e in enumerate(used)}
+    cids = np.vectorize(remap.get)(ids).astype(np.int32)
+    cols = np.unique(np.concatenate([[0, 1, wl.D - 1], synth.generator(11).choice(wl.D, 61, replace=False)]))
+    st = compact_store(wl, used)
+    want = oracle.expert_group(wl.fmt, wl.gs, st["gate"], st["gate_s"], st["up"], st["up_s"], st["down"],
+                               st["down_s"], len(used), wl.D, wl.F, x, cids, wts.astype(np.float32), cols=cols,
+                               act=1, limit=L)
+    assert max_rel(y[:, cols], want) <= GATE

@@ -124,3 +124,39 @@ def test_expert_group_routed(fmt, gs, kind, E):
     want = oracle.expert_group(fmt, g, st["gate"], st["gate_s"], st["up"], st["up_s"], st["down"], st["down_s"],
                                E, D, F, x, want_ids, want_w.astype(np.float32))
     assert max_rel(host(out), want) <= GATE
+
+
+@pytest.mark.parametrize("name", ["mxfp4_experts_E256_D6144_F2048_s1_k8", "int4_g32_experts_E256_D6144_F2048_s8_k8"])
+def test_expert_group_routed_full_size_sampled(name):
+    """The device-routed configuration the bench times: the workload's 256-expert
+    store, router logits [s][256], softmax top 8 renormalized (routing inside the
+    prep kernel).  Ids exactly the oracle's, weights within 1e-6, sampled output
+    columns against the oracle."""
+    from test_gpu_expert_group import compact_store, full_store_on_device, oracle_group
+    wl = synth.workload(name)
+    d = full_store_on_device(wl)
+    x = wl.x()
+    logits = wl.router_logits()
+    gs = wl.gs if wl.fmt == INT4_G else 0
+    ws_bytes = qexpert_group_workspace(wl.E, wl.D, wl.F, wl.s, wl.k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
+    out = empty_f32(wl.s, wl.D)
+    ids = torch.empty((wl.s, wl.k), dtype=torch.int32, device=cuda())
+    wts = torch.empty((wl.s, wl.k), dtype=torch.float32, device=cuda())
+    qexpert_group_routed(wl.fmt, gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], wl.E, wl.D,
+                         wl.F, dev(x), wl.s, wl.k, QROUTE_SOFTMAX, dev(logits), None, 1, 1.0, QACT_SWIGLU, 0.0, out,
+                         ids, wts, ws, ws_bytes, status)
+    assert int(host(status)[0]) == 0
+    want_ids, want_w = oracle.route(0, logits, k=wl.k, renorm=True)
+    assert np.array_equal(host(ids), want_ids)
+    assert np.abs(host(wts) - want_w).max() <= 1e-6 * np.abs(want_w).max()
+    y = host(out)
+    assert np.isfinite(y).all()
+    used = np.unique(want_ids)
+    remap = {int(e): i for i, e in enumerate(used)}
+    cids = np.vectorize(remap.get)(want_ids).astype(np.int32)
+    cols = np.unique(np.concatenate([[0, 1, wl.D - 1], synth.generator(7).choice(wl.D, 61, replace=False)]))
+    want = oracle_group(wl.fmt, wl.gs, compact_store(wl, used), len(used), wl.D, wl.F, x, cids,
+                        want_w.astype(np.float32), cols=cols)
+    assert max_rel(y[:, cols], want) <= GATE
