@@ -95,12 +95,14 @@ def test_gemm_agrees_with_gemv():
     assert max_rel(a, host(b)) <= 1e-5
 
 
-@pytest.mark.parametrize("s", [32, 512])
-def test_gemm_full_size_sampled(s):
-    """The int4-g32 16384 x 6144 matrix with a prefill batch, sampled rows against the oracle."""
-    wl = synth.workload("int4_g32_16384x6144_s1")
+@pytest.mark.parametrize("name", ["int4_g32_16384x6144_s32_prefill", "int4_g32_16384x6144_s512_prefill"])
+def test_gemm_full_size_sampled(name):
+    """The prefill workloads the bench times (the int4-g32 16384 x 6144 matrix,
+    32 and 512 activation rows, the same inputs), sampled rows against the oracle."""
+    wl = synth.workload(name)
     w, sc = wl.weights()
-    x = synth.draw_x(s, wl.I, synth.generator(wl.seed, 4, s))
+    x = wl.x()
+    assert wl.gemm and x.shape == (wl.s, wl.I)
     y = run_gemm(wl.fmt, wl.gs, w, sc, x, wl.O, wl.I)
     assert np.isfinite(y).all()
     rows = sample_rows(wl.O, 48)
