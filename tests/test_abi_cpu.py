@@ -402,3 +402,33 @@ def test_expert_group_checks_follow_the_header_rules(L):
         assert got in want, (fmt, gs, E, D, F, s, k, act, limit, got, want)
         seen[got] += 1
     assert min(seen[-1], seen[-2], seen[-4], seen[-9]) >= 100, dict(seen)
+
+
+def test_product_path_needs_no_oracle_and_has_no_fallback(L, tmp_path):
+    """The package imports and loads its library with the oracle made
+    unimportable; with the library missing, the first call raises instead of
+    computing anything on the host."""
+    import subprocess
+    import sys
+    pkg_dir = os.path.join(ROOT, "weight_only_quantized_qgemv_gb300")
+    for fn in os.listdir(pkg_dir):
+        if fn.endswith(".py"):
+            text = open(os.path.join(pkg_dir, fn)).read()
+            assert not re.search(r"^\s*(from|import)\s+oracle\b", text, flags=re.M), fn
+    code = (
+        "import sys\n"
+        "sys.modules['oracle'] = None\n"
+        "import weight_only_quantized_qgemv_gb300 as q\n"
+        "from weight_only_quantized_qgemv_gb300 import _build, _lib\n"
+        "assert _lib.lib() is not None\n"
+        "_lib._lib = None\n"
+        f"_build.LIB = {str(tmp_path / 'missing.so')!r}\n"
+        "try:\n"
+        "    q.qgemv(4, 32, 0, 0, 0, 16, 1024, 1, 0)\n"
+        "except RuntimeError as e:\n"
+        "    assert 'no CPU fallback' in str(e), e\n"
+        "    print('raised')\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("raised")
