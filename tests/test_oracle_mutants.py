@@ -51,6 +51,11 @@ MUTANTS = {
                              "const double sg = oracle_sigmoid((double)l[ids[t * k + r]]) + (double)bias[ids[t * k + r]];"),
     "route_sigmoid_sign": ("return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
     "route_scale_dropped": ("wts[t * k + r] = scale * exp(", "wts[t * k + r] = exp("),
+    "gemv_rows_unmapped": ("O, I, rows[j], x + t * I);", "O, I, j, x + t * I);"),
+    "gate_up_rows_unmapped": ("F, D, rows[j], x + t * D);", "F, D, j, x + t * D);"),
+    "expert_cols_unmapped": ("long d = cols ? cols[j] : j;", "long d = j;"),
+    "expert_e8m0_scale_stride": ("long ssz = fmt == ORACLE_MXFP4_E8M0 ? 1 : (long)sizeof(float);",
+                                 "long ssz = (long)sizeof(float);"),
 }
 
 
