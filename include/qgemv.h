@@ -240,7 +240,11 @@ int qdequant(int fmt, int gs, const void* w, const float* scales,
  * workspace), the MMA runs on both, and each group of gs inputs (at most 128
  * at a time) sums into a fresh f32 partial that is added to the row's sum
  * times the group scale.  The result meets the f32 GEMV's error bound, not
- * its bits.
+ * its bits.  Range: the power of two is limited to 2^-100 .. 2^100, so a row
+ * whose largest magnitude is below 2^-86 (about 1.3e-26) keeps fewer
+ * significand bits, and a row whose largest magnitude is above about 8.3e34
+ * overflows the f16 high part (its outputs are then not finite); qgemv has
+ * neither limit.
  *   w, scales, x, y as for qgemv;  workspace of ws_bytes >= qgemm_workspace(I,
  *   s) device bytes, 256-byte aligned, contents on entry irrelevant.
  * Every format, with I % 64 == 0 and groups of at least 32 inputs
