@@ -451,8 +451,21 @@ def pin_route_sigmoid_bias(orc):
     _close(w, [[s0 / (s0 + s2), s2 / (s0 + s2)]], rtol=1e-14)
 
 
+def pin_route_single_expert(orc):
+    """One expert (E = k = 1): softmax weight 1, sigmoid weight sigmoid(l) or 1 renormalized, times scale."""
+    l = np.array([[0.75], [-3.0]], np.float32)
+    ids, w = orc.route(0, l, k=1, renorm=False, scale=2.0)
+    assert ids.tolist() == [[0], [0]]
+    _close(w, [[2.0], [2.0]], rtol=1e-15)
+    ids, w = orc.route(1, l, np.array([0.3], np.float32), k=1, renorm=False, scale=2.0)
+    assert ids.tolist() == [[0], [0]]
+    _close(w, 2.0 / (1.0 + np.exp(-l.astype(np.float64))), rtol=1e-15)
+    _, w = orc.route(1, l, np.array([0.3], np.float32), k=1, renorm=True, scale=2.0)
+    _close(w, [[2.0], [2.0]], rtol=1e-15)
+
+
 ALL_PINS = [pin_e2m1, pin_e8m0, pin_int4_nibbles, pin_int3_planes, pin_int8_bytes, pin_random_codes,
             pin_format_variants,
             pin_dequant_f32, pin_fixed_groups, pin_gemv_bruteforce, pin_zero_scales, pin_linearity,
             pin_integer_exact, pin_silu, pin_clamped_glu, pin_gate_up, pin_gate_up_clamped, pin_expert_group,
-            pin_route_selection, pin_route_softmax_weights, pin_route_sigmoid_bias]
+            pin_route_selection, pin_route_softmax_weights, pin_route_sigmoid_bias, pin_route_single_expert]
