@@ -23,6 +23,7 @@ import argparse
 import glob
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -227,6 +228,9 @@ class GemvBench:
     def step(self, i, stream):
         self.call(i % self.ncopies, stream)
 
+    def period(self):
+        return self.ncopies
+
     def bytes_of(self, i):
         return self.step_bytes
 
@@ -248,7 +252,7 @@ class GemvBench:
 
 
 class ExpertBench:
-    def __init__(self, wl, device, nsteps, swiglu_limit=None, device_route=False):
+    def __init__(self, wl, device, swiglu_limit=None, device_route=False):
         import torch
         from weight_only_quantized_qgemv_gb300 import QACT_SWIGLU, QACT_SWIGLU_CLAMPED, qexpert_group_workspace
         self.wl = wl
@@ -269,7 +273,7 @@ class ExpertBench:
 
         wl.generate(range(wl.E), sink)
         torch.cuda.synchronize()
-        self.nroutes = max(64, min(nsteps, 4096))
+        self.nroutes = 64      # seeded routings the calls rotate over (each over a 6 GB store)
         ids, wts, xs = [], [], []
         for r in range(self.nroutes):
             i, w = wl.routing(step=r)
@@ -317,6 +321,9 @@ class ExpertBench:
     def step(self, i, stream):
         r = i % self.nroutes
         self._call(r, self.x[r], self.ids[r], self.wts[r], stream)
+
+    def period(self):
+        return self.nroutes
 
     def bytes_of(self, i):
         return self.route_bytes[i % self.nroutes]
@@ -474,37 +481,101 @@ def percentiles(us):
             "p90": float(np.percentile(a, 90))}
 
 
-def call_distribution(bench, graphs, G, per_call_s, stream, torch, n_replays=50, n_eager=200):
-    """µs per call as a distribution (not part of the timed region): per-replay
-    events over the CUDA graphs (each replay = G back-to-back calls), and
-    n_eager single calls each between its own pair of events.  The eager calls
-    are enqueued behind tens of milliseconds of graph replays, so the device
-    never waits on the host between them; an event between two calls also
-    keeps one call from starting early under the previous one."""
-    ng = len(graphs)
-    reps = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_replays)]
-    # enough queued device work to cover the host's enqueueing of the eager
-    # calls (tens of µs each from Python) with room to spare
-    lead = max(1, int(-(-(20e-3 + 60e-6 * n_eager) // max(per_call_s * G, 1e-9))))
+def largest_divisor_at_most(n: int, cap: int) -> int:
+    for g in range(min(n, cap), 0, -1):
+        if n % g == 0:
+            return g
+    return 1
+
+
+class GraphSet:
+    """CUDA graphs of G back-to-back calls whose replays, taken in order, continue
+    the rotation over the workload's weight copies (or routings): graph j holds
+    calls j*G .. j*G + G - 1 of an endless sequence, modulo the rotation period,
+    so no replay boundary brings a copy back sooner than the period does."""
+
+    def __init__(self, bench, G, stream, torch, max_graphs=64):
+        self.G = G
+        period = bench.period()
+        self.n = max(1, min(math.lcm(G, period) // G, max_graphs))
+        self.graphs = []
+        self.bytes = []
+        for gi in range(self.n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(G):
+                    bench.step(gi * G + j, torch.cuda.current_stream().cuda_stream)
+            self.graphs.append(g)
+            self.bytes.append(sum(bench.bytes_of(gi * G + j) for j in range(G)))
+        self.next = 0
+        with torch.cuda.stream(stream):        # warm: every graph once
+            for g in self.graphs:
+                g.replay()
+        stream.synchronize()
+
+    def replay(self):
+        """Replays the next graph of the rotation; returns the bytes its calls stream."""
+        i = self.next
+        self.graphs[i].replay()
+        self.next = (i + 1) % self.n
+        return self.bytes[i]
+
+
+def timed_regions(gs, K, stream, torch, min_regions=200, min_seconds=1.0, est_call_s=1e-5):
+    """Times regions of exactly K calls (K / G graph replays) with CUDA events on
+    the launching stream, back to back, at least min_regions of them and about
+    min_seconds in all.  Returns [(seconds, bytes)] per region."""
+    per_region = K // gs.G
+    n = max(min_regions, int(math.ceil(min_seconds / max(est_call_s * K, 1e-9))))
+    n = min(n, 200000)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    nbytes = []
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            tot = 0
+            for _ in range(per_region):
+                tot += gs.replay()
+            b.record(stream)
+            nbytes.append(tot)
+    torch.cuda.synchronize()
+    return [(a.elapsed_time(b) / 1e3, nb) for (a, b), nb in zip(evs, nbytes)]
+
+
+def eager_distribution(bench, stream, torch, per_call_s, gs, n_eager=200):
+    """Single calls, each alone between two events, enqueued behind tens of
+    milliseconds of graph replays so the device never waits on the host; the
+    event between two calls keeps one call from starting under the previous."""
+    lead = max(1, int(-(-(20e-3 + 60e-6 * n_eager) // max(per_call_s * gs.G, 1e-9))))
     calls = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_eager)]
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for r, (a, b) in enumerate(reps):
-            a.record(stream)
-            graphs[r % ng].replay()
-            b.record(stream)
-        for r in range(lead):
-            graphs[r % ng].replay()
+        for _ in range(lead):
+            gs.replay()
         for i, (a, b) in enumerate(calls):
             a.record(stream)
             bench.step(i, stream.cuda_stream)
             b.record(stream)
     torch.cuda.synchronize()
-    graph_us = [a.elapsed_time(b) * 1e3 / G for a, b in reps]
-    eager_us = [a.elapsed_time(b) * 1e3 for a, b in calls]
-    return {"graph": {"replays": n_replays, "calls_per_replay": G, "us_per_call": percentiles(graph_us)},
-            "eager": {"calls": n_eager, "us_per_call": percentiles(eager_us),
-                      "note": "each call alone between two events, behind queued work"}}
+    return percentiles([a.elapsed_time(b) * 1e3 for a, b in calls])
+
+
+def e2e_rate(bench, stream, torch, steps, world, device):
+    """The metric through the public API from pinned host buffers: every step
+    copies its inputs host -> device, calls, and reads its result back, then
+    synchronizes.  Returns (GB/s over all ranks, us per step, h2d, d2h, steps)."""
+    h2d, d2h = bench.e2e_setup()
+    barrier(world)
+    torch.cuda.synchronize()
+    nbytes = 0
+    t = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            bench.e2e_step(i, stream.cuda_stream)
+            stream.synchronize()
+            nbytes += bench.bytes_of(i)
+    dt = reduce_max(time.perf_counter() - t, world, device)
+    return reduce_sum(float(nbytes), world, device) / dt / 1e9, dt / steps * 1e6, h2d, d2h, steps
 
 
 def gemv_kernel_name(wl, sms=152):
@@ -532,6 +603,11 @@ def gemv_kernel_name(wl, sms=152):
     return "k_tile" if (shares and fits and not short) else "k_stream"
 
 
+def expert_kernel_name(wl):
+    """The launches one qexpert_group call of this workload runs."""
+    return "whole qexpert_group call (k_expert_prep + k_tile gate/up + k_tile down + k_expert_combine)"
+
+
 def gemv_config(wl):
     return {"workload": wl.name, "kind": "qgemv", "fmt": FMT_LABEL[wl.fmt] + (str(wl.gs) if wl.fmt in GROUPED else ""),
             "O": wl.O, "I": wl.I, "s": wl.s, "gs": wl.gs, "parallelism": "replicas"}
@@ -545,16 +621,74 @@ def expert_config(wl):
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
+def make_bench(wl, device, l2, swiglu_limit=None, device_route=False):
+    if isinstance(wl, synth.GemvWorkload):
+        return GemvBench(wl, device, l2)
+    return ExpertBench(wl, device, swiglu_limit, device_route)
+
+
+def est_call_seconds(wl):
+    """A rough duration of one call, to size the timed regions."""
+    if isinstance(wl, synth.GemvWorkload) and wl.gemm:
+        return 2.0 * wl.O * wl.I * wl.s / 3e14 + 30e-6
+    if isinstance(wl, synth.GemvWorkload):
+        return (wl.weight_bytes + wl.scale_bytes) / 5e12 + 2e-6
+    return 0.9 * wl.s * wl.k * wl.expert_bytes() / 5e12 + 10e-6
+
+
+def kernel_name(bench):
+    if isinstance(bench, GemvBench):
+        return gemv_kernel_name(bench.wl)
+    return expert_kernel_name(bench.wl)
+
+
+def workload_line(name, args, device, l2, stream, torch, peak, e2e_steps=200):
+    """One workload of the configs block: us per call over >= 200 timed graph
+    replays of 64 back-to-back calls, GB/s, roofline fractions, traffic and
+    the kernel, plus the same calls end to end from host buffers."""
+    wl = synth.workload(name)
+    bench = make_bench(wl, device, l2, None if isinstance(wl, synth.GemvWorkload) else args.swiglu_limit)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            bench.step(i, stream.cuda_stream)
+    stream.synchronize()
+    gs = GraphSet(bench, 64, stream, torch)
+    res = timed_regions(gs, 64, stream, torch, min_regions=200, min_seconds=0.5, est_call_s=est_call_seconds(wl))
+    us = [t / 64 * 1e6 for t, _ in res]
+    gbs = [nb / t / 1e9 for t, nb in res]
+    p = percentiles(us)
+    g50 = float(np.median(gbs))
+    e2e_gbs, e2e_us, h2d, d2h, n = e2e_rate(bench, stream, torch, e2e_steps, 1, device)
+    line = {"us_per_call": p, "GBps": g50, "frac": g50 / peak, "frac_of_8000": g50 / NOMINAL_HBM_GBS,
+            "bytes_per_call": float(np.mean([nb / 64 for _, nb in res])), "traffic": recorded_traffic(name),
+            "kernel": kernel_name(bench), "launches_per_call": bench.launches_per_step, "replays": len(res),
+            "calls_per_replay": 64,
+            "e2e": {"GBps": e2e_gbs, "us_per_call": e2e_us, "h2d_bytes": h2d, "d2h_bytes": d2h, "steps": n}}
+    if isinstance(wl, synth.GemvWorkload) and wl.gemm:
+        tpeak, _ = tensor_peak()
+        tf = 2.0 * wl.O * wl.I * wl.s / (p["p50"] * 1e-6) / 1e12
+        line.update({"bound": "tensor", "TFLOPs": tf, "frac": tf / tpeak, "frac_of_8000": None})
+    elif isinstance(wl, synth.ExpertWorkload):
+        line["us_per_fused_expert_group"] = p
+        line["mean_experts_per_call"] = float(np.mean(bench.route_bytes) / bench.expert_bytes)
+    del gs, bench
+    torch.cuda.empty_cache()
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=synth.WORKLOADS + synth.VARIANT_WORKLOADS + synth.PREFILL_WORKLOADS)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--graph-len", type=int, default=64, help="calls captured per CUDA graph replay")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload configs block")
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="configs block over the variant and prefill workloads too")
+    ap.add_argument("--min-regions", type=int, default=200, help="timed regions of --steps calls (median taken)")
     ap.add_argument("--sample-seconds", type=float, default=None,
                     help="CPU seconds per oracle sample (reference arm / CPU baseline)")
     ap.add_argument("--device-route", action="store_true",
@@ -564,15 +698,7 @@ def main():
     args = ap.parse_args()
     wl = synth.workload(args.workload)
     world, rank, local = dist_env()
-    if args.steps is None:
-        # about one second of timed device work, so the clock samples mean something
-        if isinstance(wl, synth.GemvWorkload) and wl.gemm:
-            est = 2.0 * wl.O * wl.I * wl.s / 2e14 + 30e-6
-        elif isinstance(wl, synth.GemvWorkload):
-            est = (wl.weight_bytes + wl.scale_bytes) / 6e12 + 3e-6
-        else:
-            est = 0.9 * wl.s * wl.k * wl.expert_bytes() / 6e12 + 12e-6
-        args.steps = int(min(200000, max(1000, 1.0 / est)))
+    args.steps = max(1, args.steps)
     args.warmup = max(3, args.warmup)
 
     if args.impl == "reference":
@@ -595,88 +721,72 @@ def main():
 
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024
-    bench = (GemvBench(wl, device, l2) if isinstance(wl, synth.GemvWorkload)
-             else ExpertBench(wl, device, args.steps, args.swiglu_limit, args.device_route))
+    peak, peak_src = hbm_peak()
     stream = torch.cuda.Stream(device)
+    bench = make_bench(wl, device, l2, args.swiglu_limit, args.device_route)
 
-    # warm-up: eager steps, then build the graph (its capture also warms up)
+    # warm-up: W eager steps, then the graphs (their capture and first replay warm up too)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             bench.step(i, stream.cuda_stream)
     stream.synchronize()
-    G = max(1, min(args.graph_len, args.steps))
-    graphs = []
-    period = bench.ncopies if isinstance(bench, GemvBench) else bench.nroutes
-    ngraphs = max(1, min(-(-period // G), -(-args.steps // G)))
-    for gi in range(ngraphs):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for j in range(G):
-                bench.step(gi * G + j, torch.cuda.current_stream().cuda_stream)
-        graphs.append(g)
-    with torch.cuda.stream(stream):
-        for g in graphs:
-            g.replay()
-    stream.synchronize()
+    K = args.steps
+    G = largest_divisor_at_most(K, 64)
+    gs = GraphSet(bench, G, stream, torch)
 
-    reps = -(-args.steps // G)
-    steps_done = reps * G
-    nbytes = sum(bench.bytes_of(((r % ngraphs) * G) + j) for r in range(reps) for j in range(G))
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # timed: regions of exactly K calls, at least --min-regions of them (about a
+    # second in all, so the clock samples see the load); the median region
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for r in range(reps):
-                graphs[r % ngraphs].replay()
-            ev1.record(stream)
+        res = timed_regions(gs, K, stream, torch, min_regions=args.min_regions, min_seconds=1.0,
+                            est_call_s=est_call_seconds(wl))
         torch.cuda.synchronize()
         barrier(world)
-    t_dev = ev0.elapsed_time(ev1) / 1e3
     clocks = clk.summary()
-    t_max = reduce_max(t_dev, world, device)
-    total_bytes = reduce_sum(float(nbytes), world, device)
+    times = np.array([t for t, _ in res])
+    region_bytes = np.array([nb for _, nb in res], dtype=np.float64)
+    i_med = int(np.argsort(times)[len(times) // 2])
+    t_med = float(times[i_med])
+    t_max = reduce_max(t_med, world, device)
+    total_bytes = reduce_sum(float(region_bytes[i_med]), world, device)
     value = total_bytes / t_max / 1e9
-    per_launch_s = t_dev / steps_done
-    achieved = (nbytes / steps_done) / per_launch_s / 1e9
-    peak, peak_src = hbm_peak()
-
-    timing = call_distribution(bench, graphs, G, per_launch_s, stream, torch)
+    per_launch_s = t_med / K
+    achieved = region_bytes[i_med] / K / per_launch_s / 1e9
+    timing = {"regions": len(res), "steps_per_region": K, "graph_calls_per_replay": G,
+              "us_per_call": percentiles(times / K * 1e6),
+              "timed_seconds": float(times.sum()),
+              "eager_us_per_call": eager_distribution(bench, stream, torch, per_launch_s, gs)}
 
     # end to end through the public API, host buffers, copies inside the timed region
-    h2d, d2h = bench.e2e_setup()
-    k_e2e = min(args.steps, 2000)
+    e2e_value, e2e_us, h2d, d2h, k_e2e = e2e_rate(bench, stream, torch, min(max(K, 200), 2000), world, device)
     barrier(world)
-    torch.cuda.synchronize()
-    e2e_bytes = 0
-    t = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(k_e2e):
-            bench.e2e_step(i, stream.cuda_stream)
-            stream.synchronize()
-            e2e_bytes += bench.bytes_of(i)
-    t_e2e = reduce_max(time.perf_counter() - t, world, device)
-    e2e_value = reduce_sum(float(e2e_bytes), world, device) / t_e2e / 1e9
-    barrier(world)
+    launches = bench.launches_per_step
+    kname = kernel_name(bench)
+    cfg = bench.config()
+    del gs, bench
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
         return
+
+    configs = None
+    if not args.no_configs:
+        names = list(synth.WORKLOADS) + (synth.VARIANT_WORKLOADS + synth.PREFILL_WORKLOADS
+                                         if args.all_workloads else [])
+        configs = {n: workload_line(n, args, device, l2, stream, torch, peak) for n in names}
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.sample_seconds or 12.0, args.swiglu_limit)
-    cfg = bench.config()
     cfg["graph_calls_per_replay"] = G
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_src}",
             "frac_of_8000": achieved / NOMINAL_HBM_GBS,
             "traffic": recorded_traffic(wl.name),
-            "algorithmic_bytes_per_launch": nbytes / steps_done,
-            "kernel": gemv_kernel_name(wl) if isinstance(bench, GemvBench)
-            else "whole qexpert_group call (prep + gate/up + down + combine)"}
+            "algorithmic_bytes_per_launch": float(region_bytes[i_med] / K), "kernel": kname}
     if isinstance(wl, synth.GemvWorkload) and wl.gemm:
         # a prefill batch is a dense contraction: the tensor roofline, on the
         # algorithmic 2 O I s flops (the two-part split of x doubles the MMAs)
@@ -685,19 +795,20 @@ def main():
         roof = {"bound": "tensor", "achieved": flops / per_launch_s / 1e12, "peak": tpeak, "unit": "TFLOP/s",
                 "frac": flops / per_launch_s / 1e12 / tpeak, "peak_source": tsrc,
                 "traffic": recorded_traffic(wl.name), "algorithmic_flops_per_launch": flops,
-                "mma_flops_per_launch": 2 * flops, "weight_stream_gbs": achieved,
-                "kernel": gemv_kernel_name(wl)}
+                "mma_flops_per_launch": 2 * flops, "weight_stream_gbs": achieved, "kernel": kname}
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps_done,
-        "warmup": args.warmup, "ms_per_step": t_max / steps_done * 1e3, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "us_per_call": per_launch_s * 1e6,
         "timing": timing,
         "roofline": roof,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": k_e2e, "us_per_step": t_e2e / k_e2e * 1e6},
-        "gpu_launches": steps_done * bench.launches_per_step,
+                "steps": k_e2e, "us_per_step": e2e_us},
+        "gpu_launches": K * launches,
+        "gpu_launches_all_regions": K * launches * len(res),
+        "configs": configs,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
