@@ -85,6 +85,22 @@ def test_gemm_row_scaling():
     assert np.all(np.abs(y - ystar) <= f32_bound(fmt, g, w, sc, x, O, I))
 
 
+def test_gemm_rows_at_the_range_edges():
+    """Rows near the ends of the split's range: largest magnitudes around 1e36
+    and 1e37 (the split takes p near -105 and -109) and around 1e-33 (p near
+    124) keep the f32 bound; a zero row gives zeros."""
+    fmt, gs, O, I, s = INT4_G, 32, 130, 1024, 5
+    g, w, sc, x = inputs(fmt, gs, O, I, s, 171)
+    x = x * np.array([1e36, 1e37 / 4.0, 1e-33, 3e-33, 0.0], dtype=np.float32)[:, None]
+    assert np.isfinite(x).all()
+    y = run_gemm(fmt, gs, w, sc, x, O, I)
+    ystar = oracle.qgemv(fmt, g, w, sc, x, O, I)
+    assert np.isfinite(y).all()
+    assert not y[4].any()
+    assert max_rel(y[:4], ystar[:4]) <= GATE
+    assert np.all(np.abs(y - ystar) <= f32_bound(fmt, g, w, sc, x, O, I))
+
+
 def test_gemm_agrees_with_gemv():
     """Same inputs through qgemv (groups of 8 rows) and qgemm: within the bound of each other."""
     fmt, gs, O, I, s = MXFP4_G32, 0, 300, 2048, 48

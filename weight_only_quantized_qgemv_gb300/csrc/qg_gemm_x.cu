@@ -48,10 +48,13 @@ __global__ void __launch_bounds__(256) k_gemm_split_x(const float* __restrict__ 
     for (int w = 1; w < (int)(blockDim.x >> 5); w++) amax = fmaxf(amax, red[w]);
     // amax in [2^(e-127), 2^(e-126)) for biased exponent e: p = 141 - e puts
     // it in [2^14, 2^15); zero, non-finite or subnormal maxima take p = 0 or
-    // the clamp
+    // the clamp.  p stays in [-126, 126], where 2^p and 2^-p are both normal
+    // f32: every finite row fits (FLT_MAX takes p = -113); rows below 2^-112
+    // are scaled below 2^14, where the split's error is still at most 2^-22 of
+    // each element plus 2^-25 absolute (2^-151 in x's units).
     const uint32_t e = (__float_as_uint(amax) >> 23) & 0xFFu;
-    int p = (amax == 0.f || e == 255u) ? 0 : (e == 0u ? 100 : 141 - (int)e);
-    p = p < -100 ? -100 : (p > 100 ? 100 : p);
+    int p = (amax == 0.f || e == 255u) ? 0 : (e == 0u ? 126 : 141 - (int)e);
+    p = p < -126 ? -126 : (p > 126 ? 126 : p);
     const float scale = __uint_as_float((uint32_t)(127 + p) << 23);
     for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
         float v[16];
