@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 from gpu_helpers import GATE, INT3_G64, INT4_G, INT8_ROW, MXFP4_G32, cuda, dev, empty_f32, host, max_rel, torch
+from bounds import expert_bound
 from oracle import oracle
 from test_gpu_expert_group import small_store
 from weight_only_quantized_qgemv_gb300 import (QACT_SWIGLU, QACT_SWIGLU_CLAMPED, _lib, qexpert_group_act,
@@ -140,3 +141,6 @@ def test_expert_group_clamped_full_size_sampled():
                                st["down_s"], len(used), wl.D, wl.F, x, cids, wts.astype(np.float32), cols=cols,
                                act=1, limit=L)
     assert max_rel(y[:, cols], want) <= GATE
+    b = expert_bound(wl.fmt, wl.gs, wl.gs, st, wl.D, wl.F, x, cids, wts.astype(np.float32), cols, [0], act=1,
+                     limit=L)
+    assert np.all(np.abs(y[:1, cols] - want) <= b)

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from gpu_helpers import GATE, INT3_G64, INT4_G, INT8_ROW, MXFP4_G32, cuda, dev, empty_f32, host, max_rel, torch
+from bounds import expert_bound
 from oracle import oracle
 from weight_only_quantized_qgemv_gb300 import qexpert_group, qexpert_group_workspace, synth
 
@@ -129,8 +130,13 @@ def test_expert_group_full_size_sampled(name):
     remap = {int(e): i for i, e in enumerate(used)}
     cids = np.vectorize(remap.get)(ids).astype(np.int32)
     cols = np.unique(np.concatenate([[0, 1, wl.D - 1], synth.generator(5).choice(wl.D, 61, replace=False)]))
-    want = oracle_group(wl.fmt, wl.gs, compact_store(wl, used), len(used), wl.D, wl.F, x, cids, wts, cols=cols)
+    st = compact_store(wl, used)
+    want = oracle_group(wl.fmt, wl.gs, st, len(used), wl.D, wl.F, x, cids, wts, cols=cols)
     assert max_rel(out[:, cols], want) <= GATE
+    # element by element, for the first and last token (all of them at s = 1)
+    tokens = sorted({0, wl.s - 1})
+    b = expert_bound(wl.fmt, wl.gs, wl.gs, st, wl.D, wl.F, x, cids, wts, cols, tokens)
+    assert np.all(np.abs(out[tokens][:, cols] - want[tokens]) <= b)
 
 
 def test_expert_group_most_pairs():

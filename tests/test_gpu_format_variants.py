@@ -11,6 +11,7 @@ import pytest
 
 from gpu_helpers import (GATE, INT4_ROW, INT8_G, MXFP4_E8M0, MXFP4_G32, cuda, dev, empty_f32, host, max_rel,
                          packed_rows, sample_rows, scale_rows, torch)
+from bounds import expert_bound, gemv_bound
 from oracle import oracle
 from test_gpu_expert_group import run_group, small_store
 from weight_only_quantized_qgemv_gb300 import (QACT_SWIGLU_CLAMPED, _lib, qdequant, qgate_up, qgate_up_act, qgemv,
@@ -220,9 +221,10 @@ def test_variant_full_size_sampled(name):
     y = run_gemv(wl.fmt, wl.gs if wl.fmt == INT8_G else 0, w, sc, x, wl.O, wl.I)
     assert np.isfinite(y).all()
     rows = sample_rows(wl.O, 96)
-    ystar = oracle.qgemv(wl.fmt, wl.gs, packed_rows(wl.fmt, w, wl.O, wl.I, rows), scale_rows(sc, wl.O, rows), x,
-                         len(rows), wl.I)
+    pw, ps = packed_rows(wl.fmt, w, wl.O, wl.I, rows), scale_rows(sc, wl.O, rows)
+    ystar = oracle.qgemv(wl.fmt, wl.gs, pw, ps, x, len(rows), wl.I)
     assert max_rel(y[:, rows], ystar) <= GATE
+    assert np.all(np.abs(y[:, rows] - ystar) <= gemv_bound(wl.fmt, wl.gs, pw, ps, x, len(rows), wl.I))
 
 
 def test_e8m0_expert_workload_full_size_sampled():
@@ -240,6 +242,8 @@ def test_e8m0_expert_workload_full_size_sampled():
     want = oracle.expert_group(wl.fmt, 32, st["gate"], st["gate_s"], st["up"], st["up_s"], st["down"], st["down_s"],
                                len(used), wl.D, wl.F, x, cids, wts, cols=cols)
     assert max_rel(out[:, cols], want) <= GATE
+    b = expert_bound(wl.fmt, 32, 32, st, wl.D, wl.F, x, cids, wts, cols, [0])
+    assert np.all(np.abs(out[:1, cols] - want) <= b)
     # the same store with its bytes expanded to f32 on the host: the same bits
     d7 = {n: (v if not n.endswith("_s") else torch.ldexp(torch.ones_like(v, dtype=torch.float32),
                                                              v.to(torch.int32) - 127)) for n, v in d.items()}

@@ -4,6 +4,7 @@ import pytest
 
 from gpu_helpers import GATE, INT3_G64, INT4_G, INT8_ROW, MXFP4_G32, dev, empty_f32, host, max_rel, \
     packed_rows, sample_rows, scale_rows
+from bounds import glu_bound
 from oracle import oracle
 from weight_only_quantized_qgemv_gb300 import qgate_up, synth
 
@@ -42,6 +43,10 @@ def test_gate_up_expert_size(fmt, scale_kind):
     x = synth.draw_x(s, D, rng)
     h = run(fmt, 32 if fmt == INT4_G else 0, wg, sg, wu, su, x, F, D)
     rows = sample_rows(F, 64)
-    hstar = oracle.qgate_up(fmt, 32, packed_rows(fmt, wg, F, D, rows), scale_rows(sg, F, rows),
-                            packed_rows(fmt, wu, F, D, rows), scale_rows(su, F, rows), x, len(rows), D)
+    pg, ps_g, pu, ps_u = (packed_rows(fmt, wg, F, D, rows), scale_rows(sg, F, rows), packed_rows(fmt, wu, F, D, rows),
+                          scale_rows(su, F, rows))
+    hstar = oracle.qgate_up(fmt, 32, pg, ps_g, pu, ps_u, x, len(rows), D)
     assert max_rel(h[:, rows], hstar) <= GATE
+    # every sampled element within the bound the pre-activation f32 sums propagate through silu
+    _, b = glu_bound(fmt, 32, pg, ps_g, pu, ps_u, x, len(rows), D)
+    assert np.all(np.abs(h[:, rows] - hstar) <= b)

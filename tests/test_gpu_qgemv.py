@@ -10,6 +10,7 @@ import pytest
 
 from gpu_helpers import GATE, INT3_G64, INT4_G, INT8_ROW, MXFP4_G32, dev, empty_f32, host, max_rel, \
     packed_rows, sample_rows, scale_rows
+from bounds import gemv_bound
 from oracle import oracle
 from weight_only_quantized_qgemv_gb300 import qgemv, synth
 
@@ -91,9 +92,11 @@ def test_qgemv_full_size_sampled(name):
     y = run_gemv(wl.fmt, wl.gs if wl.fmt == INT4_G else 0, w, sc, x, wl.O, wl.I)
     assert np.isfinite(y).all()
     rows = sample_rows(wl.O, 96)
-    ystar = oracle.qgemv(wl.fmt, wl.gs, packed_rows(wl.fmt, w, wl.O, wl.I, rows), scale_rows(sc, wl.O, rows), x,
-                         len(rows), wl.I)
+    pw, ps = packed_rows(wl.fmt, w, wl.O, wl.I, rows), scale_rows(sc, wl.O, rows)
+    ystar = oracle.qgemv(wl.fmt, wl.gs, pw, ps, x, len(rows), wl.I)
     assert max_rel(y[:, rows], ystar) <= GATE
+    # and every sampled element within the f32 dot-product bound of its own row
+    assert np.all(np.abs(y[:, rows] - ystar) <= gemv_bound(wl.fmt, wl.gs, pw, ps, x, len(rows), wl.I))
 
 
 def test_qgemv_full_size_repeatable():
