@@ -79,3 +79,48 @@ def test_expert_group_ring_and_tile_agree(fmt, gs, E, s, k):
     assert np.array_equal(out_ring.view(np.uint32), out_tile.view(np.uint32))
     want = oracle_group(fmt, synth.fixed_group(fmt, D, gs or None), st, E, D, F, x, ids, wts)
     assert max_rel(out_tile, want) <= GATE
+
+
+ROW_SHAPES = [(INT8_ROW, 0, 1024), (INT8_ROW, 0, 2048), (INT4_G, 32, 1024), (INT4_G, 32, 6144), (INT4_G, 64, 2048),
+              (INT4_G, 128, 4096), (INT3_G64, 0, 2048), (INT3_G64, 0, 16384), (MXFP4_G32, 0, 1024),
+              (MXFP4_G32, 0, 6144)]
+
+
+@pytest.mark.parametrize("fmt,gs,I", ROW_SHAPES)
+@pytest.mark.parametrize("O", [1, 37, 301, 1000])
+def test_qgemv_row_team_kernel(fmt, gs, I, O):
+    """The row-team kernel (forced; one activation row, rows of whole warp
+    steps) against the oracle: the gate, the per-element f32 bound, and the
+    same bits on a second call."""
+    from bounds import gemv_bound
+    g, w, sc, x = inputs(fmt, gs, O, I, 1, 59)
+    y = with_policy(_lib.QKERNEL_ROW, lambda: run_gemv(fmt, gs, w, sc, x, O, I))
+    y2 = with_policy(_lib.QKERNEL_ROW, lambda: run_gemv(fmt, gs, w, sc, x, O, I))
+    ystar = oracle.qgemv(fmt, g, w, sc, x, O, I)
+    assert max_rel(y, ystar) <= GATE
+    assert np.all(np.abs(y - ystar) <= gemv_bound(fmt, g, w, sc, x, O, I))
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt,gs,D", [(INT4_G, 32, 2048), (MXFP4_G32, 0, 6144), (INT3_G64, 0, 2048),
+                                      (INT8_ROW, 0, 1024)])
+@pytest.mark.parametrize("F", [7, 130])
+def test_gate_up_row_team_kernel(fmt, gs, D, F):
+    from bounds import glu_bound
+    g = synth.fixed_group(fmt, D, gs or None)
+    rng = synth.generator(61, fmt, F, D)
+    wg, wu = synth.draw_packed(fmt, F, D, rng), synth.draw_packed(fmt, F, D, rng)
+    sg = synth.draw_scales(F, D, g, rng, "lognormal", -4.0)
+    su = synth.draw_scales(F, D, g, rng, "lognormal", -4.0)
+    x = synth.draw_x(1, D, rng)
+
+    def run():
+        h = empty_f32(1, F)
+        qgate_up(fmt, gs, dev(wg), dev(sg), dev(wu), dev(su), dev(x), F, D, 1, h)
+        return host(h)
+
+    h = with_policy(_lib.QKERNEL_ROW, run)
+    hstar = oracle.qgate_up(fmt, g, wg, sg, wu, su, x, F, D)
+    assert max_rel(h, hstar) <= GATE
+    _, b = glu_bound(fmt, g, wg, sg, wu, su, x, F, D)
+    assert np.all(np.abs(h - hstar) <= b)

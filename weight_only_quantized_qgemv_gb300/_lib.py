@@ -130,7 +130,7 @@ def qstatus_string(status: int) -> str:
     return lib().qstatus_string(status).decode()
 
 
-QKERNEL_AUTO, QKERNEL_RING, QKERNEL_TILE = 0, 1, 2
+QKERNEL_AUTO, QKERNEL_RING, QKERNEL_TILE, QKERNEL_ROW = 0, 1, 2, 3
 
 
 def qkernel_policy(policy: int) -> int:

@@ -533,10 +533,26 @@ static cudaError_t launch_tile(const Job& job, int grid, cudaStream_t st)
     return launch_pdl(kern, dim3(grid), dim3(kTileThreads), (size_t)job.tile.total, st, job);
 }
 
+#include "qg_row.cuh"
+
+// Whether the automatic choice takes the row-team kernel for one activation row.
+#ifndef QG_ROW_AUTO
+#define QG_ROW_AUTO 0
+#endif
+
 template <int NM, int S>
 static cudaError_t launch_dense(const DenseJob<NM>& job_in, int grid, size_t x_bytes, cudaStream_t st)
 {
     DenseJob<NM> job = job_in;
+    if constexpr (S == 1) {
+        // the row-team kernel wherever its plan fits (one activation row, rows of whole warp steps)
+        const int pol = kernel_policy();
+        if ((QG_ROW_AUTO && pol == QKERNEL_AUTO) || pol == QKERNEL_ROW) {
+            bool launched = false;
+            const cudaError_t e = launch_row_dense<NM, S>(job, grid, st, launched);
+            if (launched) return e;
+        }
+    }
     constexpr int R = tile_rows_per<S, NM>();
     const int I = job.m[0].I;
     const int gs = SK == SK_ROW ? I : I / job.m[0].ngrp;
