@@ -240,11 +240,9 @@ int qdequant(int fmt, int gs, const void* w, const float* scales,
  * workspace), the MMA runs on both, and each group of gs inputs (at most 128
  * at a time) sums into a fresh f32 partial that is added to the row's sum
  * times the group scale.  The result meets the f32 GEMV's error bound, not
- * its bits.  Range: the power of two is limited to 2^-100 .. 2^100, so a row
- * whose largest magnitude is below 2^-86 (about 1.3e-26) keeps fewer
- * significand bits, and a row whose largest magnitude is above about 8.3e34
- * overflows the f16 high part (its outputs are then not finite); qgemv has
- * neither limit.
+ * its bits.  Range: the power of two is limited to 2^-126 .. 2^126, so every
+ * finite activation row fits, and the split's error stays within 2^-22 of
+ * each element plus 2^-151 absolute (below f32's resolution) for every row.
  *   w, scales, x, y as for qgemv;  workspace of ws_bytes >= qgemm_workspace(I,
  *   s) device bytes, 256-byte aligned, contents on entry irrelevant.
  * Every format, with I % 64 == 0 and groups of at least 32 inputs
@@ -323,14 +321,18 @@ int qdevice_error(int clear);
  * Kernel choice for the streaming launches of this process (a tuning and
  * testing knob; the pages have no counterpart).  QKERNEL_AUTO picks
  * per shape; QKERNEL_RING forces the per-lane copy kernel; QKERNEL_TILE the
- * tensor-copy tile kernel wherever its plan fits (else the ring kernel).  Both
- * kernels give the same bits.  Returns the previous policy, or
- * QSTATUS_BAD_FMT for an unknown one (the policy is then unchanged).  Not
- * synchronized with launches in flight on other threads.
+ * tensor-copy tile kernel wherever its plan fits (else the ring kernel);
+ * QKERNEL_ROW the row-team kernel wherever its plan fits (one activation
+ * row, rows a whole number of 32-chunk warp steps; else the automatic
+ * choice).  The ring and tile kernels give the same bits; the
+ * row-team kernel sums each row in another (fixed) order.  Returns the
+ * previous policy, or QSTATUS_BAD_FMT for an unknown one (the policy is then
+ * unchanged).  Not synchronized with launches in flight on other threads.
  */
 #define QKERNEL_AUTO 0
 #define QKERNEL_RING 1
 #define QKERNEL_TILE 2
+#define QKERNEL_ROW 3
 int qkernel_policy(int policy);
 
 #ifdef __cplusplus

@@ -185,6 +185,16 @@ def test_route_checks(L):
     assert L.qexpert_group_routed(*base, 2, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws, None, None) == -10
     assert L.qexpert_group_routed(*base, 0, A, None, 1, 1.0, 5, 0.0, A, A, A, A, ws, None, None) == -9
     assert L.qexpert_group_routed(*base, 0, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws - 1, None, None) == -5
+    # more experts than the fused routing holds (the router kernel would run
+    # first): the expert group's checks still come before anything is enqueued
+    # (with no device, an enqueued router would have returned QSTATUS_LAUNCH)
+    ws512 = _lib.lib().qexpert_group_workspace(512, 6144, 2048, 8, 8)
+    big = [7, 0, A + 8, A, A, A, A, A, 512, 6144, 2048, A, 8, 8]          # gate not 16-byte aligned
+    assert L.qexpert_group_routed(*big, 0, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws512, None, None) == -3
+    big = [7, 0, A, A, A, A, A, A, 512, 6144, 2048, A, 8, 8]
+    assert L.qexpert_group_routed(*big, 0, A, None, 1, 1.0, 0, 0.0, A, A, A, A, ws512 - 1, None, None) == -5
+    assert L.qexpert_group_routed(*big, 0, A, None, 1, 1.0, 0, 0.0, A, None, A, A, ws512, None, None) == -4
+    assert L.qexpert_group_routed(*big, 0, A, None, 1, 1.0, 3, 0.0, A, A, A, A, ws512, None, None) == -9
 
 
 def test_empty_sizes_are_rejected(L):

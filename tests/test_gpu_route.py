@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 
 from gpu_helpers import GATE, MXFP4_G32, INT4_G, cuda, dev, empty_f32, host, max_rel, torch
+from bounds import expert_bound
 from oracle import oracle
 from test_gpu_expert_group import small_store
 from weight_only_quantized_qgemv_gb300 import (QACT_SWIGLU, QROUTE_SIGMOID_BIAS, QROUTE_SOFTMAX, qexpert_group_act,
@@ -157,6 +158,35 @@ def test_expert_group_routed_full_size_sampled(name):
     remap = {int(e): i for i, e in enumerate(used)}
     cids = np.vectorize(remap.get)(want_ids).astype(np.int32)
     cols = np.unique(np.concatenate([[0, 1, wl.D - 1], synth.generator(7).choice(wl.D, 61, replace=False)]))
-    want = oracle_group(wl.fmt, wl.gs, compact_store(wl, used), len(used), wl.D, wl.F, x, cids,
-                        want_w.astype(np.float32), cols=cols)
+    st = compact_store(wl, used)
+    want = oracle_group(wl.fmt, wl.gs, st, len(used), wl.D, wl.F, x, cids, want_w.astype(np.float32), cols=cols)
     assert max_rel(y[:, cols], want) <= GATE
+    # element by element against the oracle on the device's own router weights
+    w_dev = host(wts)
+    want_d = oracle_group(wl.fmt, wl.gs, st, len(used), wl.D, wl.F, x, cids, w_dev, cols=cols)
+    tokens = sorted({0, wl.s - 1})
+    b = expert_bound(wl.fmt, wl.gs, wl.gs, st, wl.D, wl.F, x, cids, w_dev, cols, tokens)
+    assert np.all(np.abs(y[tokens][:, cols] - want_d[tokens]) <= b)
+
+
+def test_expert_group_routed_rejects_before_routing():
+    """Past 256 experts the router is a launch of its own; a call the expert
+    group would reject (here a gate not 16-byte aligned) is rejected before
+    the router is enqueued: the routing outputs stay untouched."""
+    from weight_only_quantized_qgemv_gb300 import QStatusError
+    fmt, E, D, F, s, k = MXFP4_G32, 512, 256, 128, 3, 4
+    st = small_store(fmt, E, D, F, 199)
+    d = {n: dev(v) for n, v in st.items()}
+    gate_off = torch.empty(d["gate"].numel() + 16, dtype=torch.uint8, device=cuda())[8:8 + d["gate"].numel()]
+    logits = dev(synth.generator(211).standard_normal((s, E)).astype(np.float32))
+    ws_bytes = qexpert_group_workspace(E, D, F, s, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    out = empty_f32(s, D)
+    ids = torch.full((s, k), -77, dtype=torch.int32, device=cuda())
+    wts = torch.full((s, k), -7.0, dtype=torch.float32, device=cuda())
+    with pytest.raises(QStatusError) as e:
+        qexpert_group_routed(fmt, 0, gate_off, d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], E, D, F,
+                             dev(synth.draw_x(s, D, synth.generator(213))), s, k, QROUTE_SOFTMAX, logits, None, 1,
+                             1.0, QACT_SWIGLU, 0.0, out, ids, wts, ws, ws_bytes)
+    assert e.value.status == -3
+    assert (host(ids) == -77).all() and (host(wts) == -7.0).all()

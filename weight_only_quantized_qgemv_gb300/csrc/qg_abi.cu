@@ -361,7 +361,8 @@ const char* qlast_cuda_error(void) { return g_last_cuda_error; }
 
 int qkernel_policy(int policy)
 {
-    if (policy != QKERNEL_AUTO && policy != QKERNEL_RING && policy != QKERNEL_TILE) return QSTATUS_BAD_FMT;
+    if (policy != QKERNEL_AUTO && policy != QKERNEL_RING && policy != QKERNEL_TILE && policy != QKERNEL_ROW)
+        return QSTATUS_BAD_FMT;
     return g_kernel_policy.exchange(policy);
 }
 
@@ -482,18 +483,18 @@ int qexpert_group_act(int fmt, int gs, const void* gate, const float* gate_s, co
 
 }  // extern "C"
 
-static int expert_group_impl(int fmt, int gs, const void* gate, const float* gate_s, const void* up,
-                             const float* up_s, const void* down, const float* down_s, int E, int D, int F,
-                             const float* x, int s, int k, const int32_t* ids, const float* wts, int act, float limit,
-                             float* out, void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream,
-                             const FusedRoute* route)
+// Every host-side check of the expert group (the same for the routed call,
+// which runs it before it enqueues the router).
+static int expert_checks(int fmt, int gs, const void* gate, const float* gate_s, const void* up, const float* up_s,
+                         const void* down, const float* down_s, int E, int D, int F, const float* x, int s, int k,
+                         const int32_t* ids, const float* wts, int act, float limit, const float* out,
+                         const void* workspace, size_t ws_bytes, const int32_t* status_dev, int* g_up, int* g_dn)
 {
     int st = check_act(act, limit);
     if (st) return st;
-    int g_up = 0, g_dn = 0;
-    st = check_fmt(fmt, gs, D, &g_up);
+    st = check_fmt(fmt, gs, D, g_up);
     if (st) return st;
-    st = check_fmt(fmt, gs, F, &g_dn);
+    st = check_fmt(fmt, gs, F, g_dn);
     if (st) return st;
     if (E < 1 || D < 1 || F < 1 || s < 1 || k < 1 || D > kMaxI || F > kMaxI) return QSTATUS_BAD_DIM;
     if ((long long)s * k > kMaxPairs) return QSTATUS_BAD_DIM;
@@ -504,6 +505,19 @@ static int expert_group_impl(int fmt, int gs, const void* gate, const float* gat
         !aligned(ids, 4) || !aligned(wts, 4) || !aligned(out, 4) || (status_dev && !aligned(status_dev, 4)))
         return QSTATUS_MISALIGNED;
     if (ws_bytes < ws_layout(D, F, s, k).total) return QSTATUS_WORKSPACE;
+    return QSTATUS_OK;
+}
+
+static int expert_group_impl(int fmt, int gs, const void* gate, const float* gate_s, const void* up,
+                             const float* up_s, const void* down, const float* down_s, int E, int D, int F,
+                             const float* x, int s, int k, const int32_t* ids, const float* wts, int act, float limit,
+                             float* out, void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream,
+                             const FusedRoute* route)
+{
+    int g_up = 0, g_dn = 0;
+    int st = expert_checks(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, act, limit, out,
+                           workspace, ws_bytes, status_dev, &g_up, &g_dn);
+    if (st) return st;
     int status = QSTATUS_OK;
     int grid = sm_count(&status);
     if (status) return status;
@@ -581,17 +595,15 @@ int qexpert_group_routed(int fmt, int gs, const void* gate, const float* gate_s,
                          int act, float limit, float* out, int32_t* ids_out, float* wts_out, void* workspace,
                          size_t ws_bytes, int32_t* status_dev, void* stream)
 {
-    // every host-side check of the expert group first, so a rejected call enqueues nothing
-    int g = 0;
-    int st = check_act(act, limit);
+    // every host-side check of the expert group first (with the routing outputs
+    // as its ids and weights), so a rejected call enqueues nothing
+    int g_up = 0, g_dn = 0;
+    int st = expert_checks(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids_out, wts_out, act,
+                           limit, out, workspace, ws_bytes, status_dev, &g_up, &g_dn);
     if (st) return st;
-    if ((st = check_fmt(fmt, gs, D, &g)) || (st = check_fmt(fmt, gs, F, &g))) return st;
-    if (E < 1 || D < 1 || F < 1 || s < 1 || k < 1 || D > kMaxI || F > kMaxI) return QSTATUS_BAD_DIM;
-    if ((long long)s * k > kMaxPairs) return QSTATUS_BAD_DIM;
-    if (!workspace) return QSTATUS_NULL;
-    if (ws_bytes < ws_layout(D, F, s, k).total) return QSTATUS_WORKSPACE;
     if (E > kFusedRouteMaxE) {
-        // more experts than the prep kernel's fused routing holds: the router kernel first
+        // more experts than the prep kernel's fused routing holds: the router
+        // kernel first (qroute checks its own arguments before it enqueues)
         st = qroute(route_kind, logits, bias, s, E, k, renorm, route_scale, ids_out, wts_out, stream);
         if (st) return st;
         return qexpert_group_act(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids_out, wts_out,

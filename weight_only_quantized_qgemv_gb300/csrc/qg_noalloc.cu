@@ -7,6 +7,8 @@
 // array compiled into the library: every GPU that loads the library holds
 // QEXPERT_NOALLOC_SCRATCH_BYTES of it until the process exits.  The caller
 // still passes the inputs and the output.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "qg_internal.h"
@@ -16,8 +18,10 @@
 static __device__ __align__(256) unsigned char g_expert_scratch[QEXPERT_NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_expert_scratch on each device, looked up at the first
-// call made with that device current.
-static void* g_scratch_addr[64];
+// call made with that device current.  Atomic, so host threads making their
+// first call on a device at the same time do not race (they store the same
+// address).  A cudaDeviceReset invalidates it: reload the library after one.
+static std::atomic<void*> g_scratch_addr[64];
 
 extern "C" int qexpert_group_noalloc(int fmt, int gs, const void* gate, const float* gate_s, const void* up,
                                      const float* up_s, const void* down, const float* down_s, int E, int D, int F,
@@ -28,11 +32,12 @@ extern "C" int qexpert_group_noalloc(int fmt, int gs, const void* gate, const fl
     if (need > (size_t)QEXPERT_NOALLOC_SCRATCH_BYTES) return QSTATUS_WORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QSTATUS_LAUNCH;
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_expert_scratch) != cudaSuccess || p == nullptr) return QSTATUS_LAUNCH;
-        g_scratch_addr[dev] = p;
+    void* scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (scratch == nullptr) {
+        if (cudaGetSymbolAddress(&scratch, g_expert_scratch) != cudaSuccess || scratch == nullptr)
+            return QSTATUS_LAUNCH;
+        g_scratch_addr[dev].store(scratch, std::memory_order_release);
     }
-    return qexpert_group(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, out,
-                         g_scratch_addr[dev], (size_t)QEXPERT_NOALLOC_SCRATCH_BYTES, status_dev, stream);
+    return qexpert_group(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, out, scratch,
+                         (size_t)QEXPERT_NOALLOC_SCRATCH_BYTES, status_dev, stream);
 }

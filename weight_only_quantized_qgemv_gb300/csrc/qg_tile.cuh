@@ -292,9 +292,11 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
     }
     if (!ok) {
         tile_fail(status);
-        // the CTA must not retire while copies into its shared memory are in flight
+        // the CTA must not retire while copies into its shared memory are in
+        // flight: wait for every slot issued and not yet consumed, each wait
+        // bounded, without stopping at one that runs out
         for (; consumed < issued; consumed++) {
-            if (!mbar_wait(full0 + 8u * (uint32_t)slot, phase)) break;
+            (void)mbar_wait(full0 + 8u * (uint32_t)slot, phase);
             if (++slot == P) {
                 slot = 0;
                 phase ^= 1u;
