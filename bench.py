@@ -288,12 +288,14 @@ class ExpertBench:
         self.x = torch.from_numpy(self.x_host).to(device)
         self.out = torch.empty(wl.s, wl.D, dtype=torch.float32, device=device)
         self.ws_bytes = qexpert_group_workspace(wl.E, wl.D, wl.F, wl.s, wl.k)
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)   # zeroed before first use
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.gs = wl.gs if wl.fmt in GROUPED else 0
         self.expert_bytes = wl.expert_bytes()
         self.route_bytes = [len(np.unique(self.ids_host[r])) * self.expert_bytes for r in range(self.nroutes)]
-        self.launches_per_step = 4
+        # one persistent launch up to 256 (token, rank) pairs, else prep, gate/up, down, combine
+        self.fused = wl.s * wl.k <= 256
+        self.launches_per_step = 1 if self.fused else 4
         self.device_route = device_route
         if device_route:
             # routing on the device from seeded logits: softmax top-k, renormalized
@@ -303,7 +305,8 @@ class ExpertBench:
             self.wts_out = torch.empty(wl.s, wl.k, dtype=torch.float32, device=device)
             top = np.argpartition(-self.logits_host, wl.k - 1, axis=2)[:, :, :wl.k]
             self.route_bytes = [len(np.unique(top[r])) * self.expert_bytes for r in range(self.nroutes)]
-            self.launches_per_step = 4 if wl.E <= 256 else 5   # routing fused into the prep kernel up to 256 experts
+            if wl.E > 256:                                     # a router launch of its own ahead
+                self.launches_per_step += 1
 
     def _call(self, r, x, ids, wts, stream, logits=None):
         from weight_only_quantized_qgemv_gb300 import QROUTE_SOFTMAX, qexpert_group_act, qexpert_group_routed
@@ -605,6 +608,8 @@ def gemv_kernel_name(wl, sms=152):
 
 def expert_kernel_name(wl):
     """The launches one qexpert_group call of this workload runs."""
+    if wl.s * wl.k <= 256:
+        return "k_moe (the whole expert group in one launch)"
     return "whole qexpert_group call (k_expert_prep + k_tile gate/up + k_tile down + k_expert_combine)"
 
 

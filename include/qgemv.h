@@ -148,7 +148,10 @@ int qgate_up_act(int fmt, int gs, const void* wg, const float* sg,
                  const void* wu, const float* su,
                  const float* x, int F, int D, int s, int act, float limit, float* h, void* stream);
 
-/* Bytes of workspace qexpert_group needs for these sizes. */
+/* Bytes of workspace qexpert_group needs for these sizes.  The workspace
+ * must hold zeros before its first use (cudaMemset it once after allocating
+ * it); every call leaves it that way -- its first words are the counters of
+ * the one-launch expert group's grid barriers. */
 size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
 
 /*
@@ -162,12 +165,19 @@ size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
  *   x         f32 [s][D];  ids int32 [s][k];  wts f32 [s][k]
  *   out       f32 [s][D], written
  *   workspace device scratch of ws_bytes >= qexpert_group_workspace(E, D, F, s, k)
- *             bytes, 256-byte aligned; its contents on entry do not matter.
+ *             bytes, 256-byte aligned, zeroed before its first use (see
+ *             qexpert_group_workspace); calls leave it zeroed.
  *   status_dev optional device int32: set to QSTATUS_OK, or to
  *             QSTATUS_BAD_EXPERT_ID when an id is outside [0, E) -- then out is
- *             all zeros.  The host-side return cannot see device-side checks.
- * Each expert's weights are streamed once for all the (token, rank) pairs
- * routed to it; repeated ids in a row are allowed and summed.  s * k <= 4096.
+ *             all zeros -- or to QSTATUS_DEVICE_TIMEOUT when a bounded wait of
+ *             the launch ran out.  The host-side return cannot see device-side
+ *             checks.
+ * Up to 256 (token, rank) pairs the call is one persistent launch (gate/up,
+ * act, down and the rank-order sum; its CTAs, one per SM, meet at two grid
+ * barriers, so the launch needs every SM of the device at once); past that,
+ * and under QKERNEL_RING or QKERNEL_TILE, four launches that stream each
+ * expert's weights once for all the pairs routed to it.  Repeated ids in a row
+ * are allowed and summed.  s * k <= 4096.
  */
 int qexpert_group(int fmt, int gs,
                   const void* gate, const float* gate_s,
@@ -206,10 +216,11 @@ int qexpert_group_act(int fmt, int gs,
  * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Every call on a device shares the one array and leaves its
- * contents behind; nothing in it needs clearing, since each call writes every
- * scratch word it later reads.  Calls that overlap on the GPU (other streams,
- * other host threads) race on the array: serialize them.
+ * stream capture.  Every call on a device shares the one array: it starts
+ * zeroed when the library loads, and each call leaves the words that must be
+ * zero (the grid-barrier counters) zeroed and writes every other scratch word
+ * before it reads it.  Calls that overlap on the GPU (other streams, other
+ * host threads) race on the array: serialize them.
  */
 #define QEXPERT_NOALLOC_SCRATCH_BYTES (4u << 20)
 
@@ -301,6 +312,21 @@ int qexpert_group_routed(int fmt, int gs,
                          int act, float limit,
                          float* out, int32_t* ids_out, float* wts_out,
                          void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * Test hook (no counterpart in the pages, whose backends inject their faults
+ * through environment switches): arms one fault for the next one-launch
+ * expert group of this process.  QDEBUG_WITHHOLD_SIGNAL makes one CTA of that
+ * launch skip its phase-A arrival, so the other CTAs' bounded waits run out
+ * after wait_ns nanoseconds: the launch records QSTATUS_DEVICE_TIMEOUT (in
+ * qdevice_error and in the call's status word), its results are undefined, it
+ * returns, and it leaves the workspace ready for the next call.  Nothing
+ * faults or waits without bound.  QDEBUG_NONE disarms.  Returns QSTATUS_OK,
+ * or QSTATUS_BAD_DIM for an unknown kind or wait_ns below 1.
+ */
+#define QDEBUG_NONE 0
+#define QDEBUG_WITHHOLD_SIGNAL 1
+int qdebug_inject(int kind, long long wait_ns);
 
 /* A static description of a status code. */
 const char* qstatus_string(int status);

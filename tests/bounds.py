@@ -39,7 +39,8 @@ def _act(g, u, act, limit):
     if act == 1:
         g = np.minimum(g, limit)
         u = np.clip(u, -limit, limit)
-    silu = g / (1.0 + np.exp(-g))
+    with np.errstate(over="ignore"):          # exp(-g) -> inf for very negative g: silu -> -0
+        silu = g / (1.0 + np.exp(-g))
     return silu, u
 
 

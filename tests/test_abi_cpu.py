@@ -197,6 +197,15 @@ def test_route_checks(L):
     assert L.qexpert_group_routed(*big, 0, A, None, 1, 1.0, 3, 0.0, A, A, A, A, ws512, None, None) == -9
 
 
+def test_debug_inject_checks(L):
+    """The test hook's arguments: unknown kinds and waits below 1 ns are refused; disarming always works."""
+    assert L.qdebug_inject(5, 1000) == -2
+    assert L.qdebug_inject(1, 0) == -2
+    assert L.qdebug_inject(0, 0) == 0
+    assert L.qdebug_inject(1, 1000000) == 0      # armed ...
+    assert L.qdebug_inject(0, 0) == 0            # ... and disarmed again (no launch happens here)
+
+
 def test_empty_sizes_are_rejected(L):
     """Zero rows, inputs or activation rows: QSTATUS_BAD_DIM before anything is enqueued."""
     assert L.qgemv(4, 32, A, A, A, 0, 1024, 1, A, None) == -2

@@ -81,7 +81,7 @@ def run_group_act(fmt, gs, st, E, D, F, x, ids, wts, act, limit):
     d = {n: dev(v) for n, v in st.items()}
     out = empty_f32(s, D)
     ws_bytes = qexpert_group_workspace(E, D, F, s, k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda())   # zeroed before first use
     status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
     qexpert_group_act(fmt, gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], E, D, F,
                       dev(x), s, k, dev(ids.astype(np.int32)), dev(wts.astype(np.float32)), act, limit, out, ws,
@@ -123,7 +123,7 @@ def test_expert_group_clamped_full_size_sampled():
     x = wl.x()
     ids, wts = wl.routing()
     ws_bytes = qexpert_group_workspace(wl.E, wl.D, wl.F, wl.s, wl.k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda())   # zeroed before first use
     status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
     out = empty_f32(wl.s, wl.D)
     qexpert_group_act(wl.fmt, 0, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], wl.E, wl.D,

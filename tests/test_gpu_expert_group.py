@@ -33,7 +33,7 @@ def run_group(fmt, gs, st, E, D, F, x, ids, wts, stores_on_device=None):
     d = stores_on_device or {n: dev(v) for n, v in st.items()}
     out = empty_f32(s, D)
     ws_bytes = qexpert_group_workspace(E, D, F, s, k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda())   # zeroed before first use
     status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
     qexpert_group(fmt, gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], E, D, F,
                   dev(x), s, k, dev(ids.astype(np.int32)), dev(wts.astype(np.float32)), out, ws, ws_bytes, status)

@@ -105,7 +105,7 @@ def test_expert_group_routed(fmt, gs, kind, E):
     bias = (0.3 * rng.standard_normal(E)).astype(np.float32)
     d = {n: dev(v) for n, v in st.items()}
     ws_bytes = qexpert_group_workspace(E, D, F, s, k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda())   # zeroed before first use
     status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
     out = empty_f32(s, D)
     ids = torch.empty((s, k), dtype=torch.int32, device=cuda())
@@ -140,7 +140,7 @@ def test_expert_group_routed_full_size_sampled(name):
     logits = wl.router_logits()
     gs = wl.gs if wl.fmt == INT4_G else 0
     ws_bytes = qexpert_group_workspace(wl.E, wl.D, wl.F, wl.s, wl.k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda())   # zeroed before first use
     status = torch.full((1,), 12345, dtype=torch.int32, device=cuda())
     out = empty_f32(wl.s, wl.D)
     ids = torch.empty((wl.s, wl.k), dtype=torch.int32, device=cuda())
@@ -180,7 +180,7 @@ def test_expert_group_routed_rejects_before_routing():
     gate_off = torch.empty(d["gate"].numel() + 16, dtype=torch.uint8, device=cuda())[8:8 + d["gate"].numel()]
     logits = dev(synth.generator(211).standard_normal((s, E)).astype(np.float32))
     ws_bytes = qexpert_group_workspace(E, D, F, s, k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda())   # zeroed before first use
     out = empty_f32(s, D)
     ids = torch.full((s, k), -77, dtype=torch.int32, device=cuda())
     wts = torch.full((s, k), -7.0, dtype=torch.float32, device=cuda())

@@ -48,7 +48,7 @@ def test_noalloc_matches_workspace_entry_point_twice(fmt, gs):
         ids, wts = dev(ids_np), dev(wts_np)
         out_ref = empty_f32(s, D)
         ws_bytes = qexpert_group_workspace(E, D, F, s, k)
-        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda())
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda())   # zeroed before first use
         qexpert_group(fmt, gs, d["gate"], d["gate_s"], d["up"], d["up_s"], d["down"], d["down_s"], E, D, F,
                       x, s, k, ids, wts, out_ref, ws, ws_bytes)
         out = empty_f32(s, D)

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.qdevice_error.restype = I
         L.qkernel_policy.argtypes = [I]
         L.qkernel_policy.restype = I
+        L.qdebug_inject.argtypes = [I, ctypes.c_longlong]
+        L.qdebug_inject.restype = I
         _lib = L
     return _lib
 
@@ -139,6 +141,14 @@ def qkernel_policy(policy: int) -> int:
     if prev < 0:
         raise QStatusError(prev, qstatus_string(prev))
     return prev
+
+
+QDEBUG_NONE, QDEBUG_WITHHOLD_SIGNAL = 0, 1
+
+
+def qdebug_inject(kind: int, wait_ns: int = 1) -> None:
+    """Arms a test fault for the next one-launch expert group (QDEBUG_*)."""
+    _check(lib().qdebug_inject(int(kind), int(wait_ns)))
 
 
 def qdevice_error(clear: bool = False) -> int:

@@ -16,6 +16,11 @@ static thread_local const char* g_last_cuda_error = "no error";
 static std::atomic<int> g_kernel_policy{QKERNEL_AUTO};
 int kernel_policy() { return g_kernel_policy.load(std::memory_order_relaxed); }
 
+// The armed test fault (qdebug_inject) and its wait bound, consumed by the
+// next fused expert-group launch.
+static std::atomic<int> g_inject{QDEBUG_NONE};
+static std::atomic<long long> g_inject_ns{0};
+
 static int launch_status(cudaError_t e)
 {
     if (e == cudaSuccess) return QSTATUS_OK;
@@ -359,6 +364,18 @@ const char* qstatus_string(int status)
 
 const char* qlast_cuda_error(void) { return g_last_cuda_error; }
 
+int qdebug_inject(int kind, long long wait_ns)
+{
+    if (kind == QDEBUG_NONE) {
+        g_inject.store(QDEBUG_NONE);
+        return QSTATUS_OK;
+    }
+    if (kind != QDEBUG_WITHHOLD_SIGNAL || wait_ns < 1) return QSTATUS_BAD_DIM;
+    g_inject_ns.store(wait_ns);
+    g_inject.store(kind);
+    return QSTATUS_OK;
+}
+
 int qkernel_policy(int policy)
 {
     if (policy != QKERNEL_AUTO && policy != QKERNEL_RING && policy != QKERNEL_TILE && policy != QKERNEL_ROW)
@@ -560,7 +577,21 @@ static int expert_group_impl(int fmt, int gs, const void* gate, const float* gat
     if (a.smax < 1) return QSTATUS_BAD_DIM;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
-    cudaError_t e = expert_prep(a, cs);
+    cudaError_t e = cudaSuccess;
+    const int pol = kernel_policy();
+    if ((pol == QKERNEL_AUTO || pol == QKERNEL_ROW) && (long long)s * k <= kFusedMaxPairs) {
+        // one persistent launch: routing (optional), gate/up, down and the rank-order sum
+        if (g_inject.exchange(QDEBUG_NONE) == QDEBUG_WITHHOLD_SIGNAL) {
+            a.withhold = 1;
+            a.wait_ns = (unsigned long long)g_inject_ns.load();
+        }
+        bool launched = false;
+#define QG_CALL(name) expert_fused_##name(a, grid, cs, &launched)
+        QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+        if (launched || e != cudaSuccess) return launch_status(e);
+    }
+    e = expert_prep(a, cs);
     if (e != cudaSuccess) return launch_status(e);
 #define QG_CALL(name) expert_up_##name(a, grid, cs)
     QG_FMT_SWITCH(fmt, QG_CALL)

@@ -9,6 +9,7 @@
 
 #include "qg_device.cuh"
 #include "qg_internal.h"
+#include "qg_route.cuh"
 
 #ifndef QG_FMT
 #error "define QG_FMT and QG_NAME before including qg_fmt_impl.cuh"
@@ -535,6 +536,8 @@ static cudaError_t launch_tile(const Job& job, int grid, cudaStream_t st)
 
 #include "qg_row.cuh"
 
+#include "qg_moe.cuh"
+
 // Whether the automatic choice takes the row-team kernel for one activation row.
 #ifndef QG_ROW_AUTO
 #define QG_ROW_AUTO 0
@@ -735,6 +738,57 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
         if (e != cudaSuccess) return e;
         return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, job);
     });
+}
+
+cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st, bool* launched)
+{
+    *launched = false;
+    const int gs_up = SK == SK_ROW ? a.D : a.gs, gs_dn = SK == SK_ROW ? a.F : a.gs;
+    MoeJob job;
+    job.gate0 = to_mat(HostMat{a.gate, a.gate_s, a.F, a.D, gs_up});
+    job.up0 = to_mat(HostMat{a.up, a.up_s, a.F, a.D, gs_up});
+    job.down0 = to_mat(HostMat{a.down, a.down_s, a.D, a.F, gs_dn});
+    if (!plan_moe(a.D, a.F, job.gate0.gsh, job.down0.gsh, job.plan)) return cudaSuccess;
+    const long long D = a.D, F = a.F;
+    job.rbA = code_row_bytes(a.D);
+    job.rbA_B = FMT == FMT_INT3_G64 ? D / 8 : 0;
+    job.sbA = SK == SK_ROW ? 0 : (SK == SK_E8M0 ? job.gate0.ngrp : 4ll * job.gate0.ngrp);
+    job.rbB = code_row_bytes(a.F);
+    job.rbB_B = FMT == FMT_INT3_G64 ? F / 8 : 0;
+    job.sbB = SK == SK_ROW ? 0 : (SK == SK_E8M0 ? job.down0.ngrp : 4ll * job.down0.ngrp);
+    job.up_bytes = F * job.rbA + F * job.rbA_B;
+    job.dn_bytes = D * job.rbB + D * job.rbB_B;
+    job.up_scales = F * job.gate0.ngrp;
+    job.dn_scales = D * job.down0.ngrp;
+    const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
+    job.x = a.x;
+    job.ids = a.ids;
+    job.wts = a.wts;
+    job.out = a.out;
+    job.h = reinterpret_cast<float*>(a.ws + L.h);
+    job.z = reinterpret_cast<float*>(a.ws + L.z);
+    job.ctr = reinterpret_cast<unsigned*>(a.ws + L.hdr) + 4;
+    job.status = a.status_dev;
+    job.E = a.E;
+    job.D = a.D;
+    job.F = a.F;
+    job.s = a.s;
+    job.k = a.k;
+    job.P = a.s * a.k;
+    job.act = a.act;
+    job.limit = a.limit;
+    job.wait_ns = a.wait_ns;
+    job.withhold = a.withhold;
+    job.route_kind = a.route_kind;
+    job.logits = a.logits;
+    job.bias = a.bias;
+    job.renorm = a.renorm;
+    job.route_scale = a.route_scale;
+    static int granted[64];
+    cudaError_t e = set_smem(k_moe<FMT>, (size_t)job.plan.total, granted);
+    if (e != cudaSuccess) return e;
+    *launched = true;
+    return launch_pdl(k_moe<FMT>, dim3(grid), dim3(kMoeThreads), (size_t)job.plan.total, st, job);
 }
 
 int QG_CAT(device_error_, QG_NAME)(int clear)

@@ -90,7 +90,14 @@ struct ExpertArgs {
     const float* bias = nullptr;
     int renorm = 0;
     float route_scale = 1.0f;
+    // the fused launch: bound of its device waits, and the test hook that
+    // withholds one CTA's phase-A signal
+    unsigned long long wait_ns = 2000000000ull;
+    int withhold = 0;
 };
+
+// Pairs (s * k) up to which qexpert_group runs as one fused launch.
+constexpr int kFusedMaxPairs = 256;
 
 constexpr int kFusedRouteMaxE = 256;   // experts the prep kernel's fused routing holds (8 per lane)
 
@@ -174,6 +181,7 @@ cudaError_t route_launch(int kind, const float* logits, const float* bias, int s
                                long long ldh, int act, float limit, int grid, cudaStream_t st);        \
     cudaError_t expert_up_##name(const ExpertArgs& a, int grid, cudaStream_t st);                       \
     cudaError_t expert_down_##name(const ExpertArgs& a, int grid, cudaStream_t st);                     \
+    cudaError_t expert_fused_##name(const ExpertArgs& a, int grid, cudaStream_t st, bool* launched);    \
     cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);                         \
     cudaError_t gemm_##name(const HostMat& m, const GemmArgs& g, cudaStream_t st);                     \
     size_t ring_bytes_##name(int nm);                                                                 \
