@@ -189,6 +189,17 @@ int qexpert_group(int fmt, int gs,
                   float* out, void* workspace, size_t ws_bytes,
                   int32_t* status_dev, void* stream);
 
+/*
+ * How many kernel launches qexpert_group (routed = 0) or qexpert_group_routed
+ * (routed != 0) makes for these sizes on the current device under the
+ * current qkernel_policy: 1 when the call runs as the one fused launch, 4
+ * for the four-launch path (pair sort, gate/up, down, rank-order sum), plus
+ * 1 for the router kernel of a routed call with E > 256.  Nothing is
+ * enqueued.  Negative QSTATUS_* for sizes or a format the call rejects, or
+ * when no device is usable.
+ */
+int qexpert_group_launches(int fmt, int gs, int E, int D, int F, int s, int k, int routed);
+
 /* qexpert_group with the activation act (QACT_*) and its limit in place of
  * silu(g) * u; QSTATUS_BAD_ACT as for qgate_up_act. */
 int qexpert_group_act(int fmt, int gs,

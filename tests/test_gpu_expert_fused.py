@@ -1,8 +1,9 @@
-"""The routed-expert group as one persistent launch (up to 256 pairs, rows of
-whole warp steps) against the f64 oracle: every format, repeated experts in a
-row, bad ids, the workspace reused call after call (its barrier counters must
-come back to zero), routing inside the launch, the four-launch path for
-comparison, and a bounded device wait made to run out on purpose."""
+"""The routed-expert group as one persistent launch (up to 256 pairs) against
+the f64 oracle: every format, ragged row lengths, repeated experts in a row,
+bad ids, the workspace reused call after call (its barrier counters must come
+back to zero), routing inside the launch, the four-launch path (the same
+streaming passes, so the same bits), the launch count the library reports,
+and a bounded device wait made to run out on purpose."""
 import numpy as np
 import pytest
 
@@ -12,7 +13,8 @@ from gpu_helpers import (GATE, INT3_G64, INT4_G, INT4_ROW, INT8_G, INT8_ROW, MXF
 from oracle import oracle
 from test_gpu_expert_group import oracle_group, small_store
 from weight_only_quantized_qgemv_gb300 import (QACT_SWIGLU, QROUTE_SOFTMAX, _lib, qexpert_group,
-                                               qexpert_group_routed, qexpert_group_workspace, synth)
+                                               qexpert_group_launches, qexpert_group_routed, qexpert_group_workspace,
+                                               synth)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,9 +41,10 @@ def routing(rng, s, k, E, repeats):
 
 
 FMTS = [(INT4_G, 32), (MXFP4_G32, 0), (INT8_ROW, 0), (INT3_G64, 0), (INT4_ROW, 0), (INT8_G, 32), (MXFP4_E8M0, 0)]
-# (E, D, F, s, k): D and F whole warp steps of chunks (int3: 2048 inputs)
+# (E, D, F, s, k): several row tiles and slices, ragged rows (640 and 1152
+# inputs end inside a slice), 256 pairs
 SHAPES = [(5, 2048, 2048, 1, 1), (9, 2048, 2048, 1, 4), (12, 4096, 2048, 3, 4), (64, 2048, 2048, 8, 8),
-          (7, 6144, 2048, 2, 3)]
+          (7, 6144, 2048, 2, 3), (6, 640, 1152, 3, 2), (256, 1152, 640, 32, 8)]
 
 
 @pytest.mark.parametrize("fmt,gs", FMTS)
@@ -56,6 +59,7 @@ def test_fused_matches_oracle(fmt, gs, E, D, F, s, k, repeats):
     x = synth.draw_x(s, D, rng)
     ids, wts = routing(rng, s, k, E, repeats)
     ws, nb = workspace(E, D, F, s, k)
+    assert qexpert_group_launches(fmt, gs, E, D, F, s, k) == 1
     out, status = call(fmt, gs, d, E, D, F, x, ids, wts, ws, nb)
     assert status == 0
     g_up, g_dn = synth.fixed_group(fmt, D, gs or None), synth.fixed_group(fmt, F, gs or None)   # row formats: I
@@ -67,9 +71,11 @@ def test_fused_matches_oracle(fmt, gs, E, D, F, s, k, repeats):
     assert np.all(np.abs(out[tokens][:, cols] - want[tokens][:, cols]) <= b)
 
 
-def test_fused_against_four_launch_path():
-    """The same call through the four-launch path (QKERNEL_TILE): both within the gate of each other."""
-    fmt, gs, E, D, F, s, k = MXFP4_G32, 0, 16, 2048, 2048, 4, 4
+@pytest.mark.parametrize("fmt,gs", FMTS)
+def test_fused_against_four_launch_path(fmt, gs):
+    """The same call through the four-launch path (QKERNEL_TILE): the same
+    streaming passes and the same rank-order sum, so the same bits."""
+    E, D, F, s, k = 16, 2048, 1152, 4, 4
     st = small_store(fmt, E, D, F, 307)
     d = {n: dev(v) for n, v in st.items()}
     rng = synth.generator(309)
@@ -79,14 +85,28 @@ def test_fused_against_four_launch_path():
     fused, st1 = call(fmt, gs, d, E, D, F, x, ids, wts, ws, nb)
     prev = _lib.qkernel_policy(_lib.QKERNEL_TILE)
     try:
+        assert qexpert_group_launches(fmt, gs, E, D, F, s, k) == 4
         four, st2 = call(fmt, gs, d, E, D, F, x, ids, wts, ws, nb)
     finally:
         _lib.qkernel_policy(prev)
     assert st1 == 0 and st2 == 0
-    assert max_rel(fused, four) <= 1e-5
+    assert np.array_equal(fused.view(np.uint32), four.view(np.uint32))
     # and the workspace still works for the fused launch after the other path used it
     again, st3 = call(fmt, gs, d, E, D, F, x, ids, wts, ws, nb)
     assert st3 == 0 and np.array_equal(again.view(np.uint32), fused.view(np.uint32))
+
+
+def test_launch_counts():
+    """One launch up to 256 pairs, four past that; a routed call over more than
+    256 experts adds the router kernel."""
+    assert qexpert_group_launches(INT4_G, 32, 256, 6144, 2048, 8, 8) == 1
+    assert qexpert_group_launches(MXFP4_G32, 0, 256, 6144, 2048, 1, 8) == 1
+    assert qexpert_group_launches(MXFP4_G32, 0, 256, 6144, 2048, 1, 8, routed=True) == 1
+    assert qexpert_group_launches(INT4_G, 32, 256, 2048, 2048, 32, 8) == 1
+    assert qexpert_group_launches(INT4_G, 32, 256, 2048, 2048, 33, 8) == 4
+    assert qexpert_group_launches(INT4_G, 32, 512, 2048, 2048, 4, 8, routed=True) == 2
+    with pytest.raises(_lib.QStatusError):
+        qexpert_group_launches(INT4_G, 32, 256, 2048, 2048, 0, 8)
 
 
 def test_fused_workspace_reused_call_after_call():

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.qgate_up.restype = I
         L.qexpert_group_workspace.argtypes = [I, I, I, I, I]
         L.qexpert_group_workspace.restype = Z
+        L.qexpert_group_launches.argtypes = [I, I, I, I, I, I, I, I]
+        L.qexpert_group_launches.restype = I
         L.qexpert_group.argtypes = [I, I, P, P, P, P, P, P, I, I, I, P, I, I, P, P, P, P, Z, P, P]
         L.qexpert_group.restype = I
         Fl = ctypes.c_float
@@ -173,6 +175,13 @@ def qgate_up_act(fmt, gs, wg, sg, wu, su, x, F, D, s, act, limit, h, stream=None
 
 def qexpert_group_workspace(E, D, F, s, k) -> int:
     return lib().qexpert_group_workspace(E, D, F, s, k)
+
+
+def qexpert_group_launches(fmt, gs, E, D, F, s, k, routed=False) -> int:
+    """Kernel launches of one expert-group call of these sizes (1: the fused launch)."""
+    n = lib().qexpert_group_launches(fmt, gs, E, D, F, s, k, int(bool(routed)))
+    _check(min(n, 0))
+    return n
 
 
 def qexpert_group(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, out,

@@ -525,25 +525,15 @@ static int expert_checks(int fmt, int gs, const void* gate, const float* gate_s,
     return QSTATUS_OK;
 }
 
-static int expert_group_impl(int fmt, int gs, const void* gate, const float* gate_s, const void* up,
-                             const float* up_s, const void* down, const float* down_s, int E, int D, int F,
-                             const float* x, int s, int k, const int32_t* ids, const float* wts, int act, float limit,
-                             float* out, void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream,
-                             const FusedRoute* route)
+// The launch shape of an expert group (no pointers): the grid, the batch
+// size smax and the tile counts of the four-launch path.
+static int expert_shape(int fmt, int gs_up, int E, int D, int F, int s, int k, ExpertArgs& a)
 {
-    int g_up = 0, g_dn = 0;
-    int st = expert_checks(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, act, limit, out,
-                           workspace, ws_bytes, status_dev, &g_up, &g_dn);
-    if (st) return st;
     int status = QSTATUS_OK;
     int grid = sm_count(&status);
     if (status) return status;
     if (grid > kMaxGrid) grid = kMaxGrid;
-
-    ExpertArgs a;
     a.grid = grid;
-    a.act = act;
-    a.limit = limit;
     int r_up = 1, r_dn = 1;
     switch (fmt) {
     case QFMT_INT8_ROW: r_up = tile_rows_int8(2); r_dn = tile_rows_int8(1); break;
@@ -556,10 +546,48 @@ static int expert_group_impl(int fmt, int gs, const void* gate, const float* gat
     }
     a.tpb_up = (F + r_up - 1) / r_up;
     a.tpb_down = (D + r_dn - 1) / r_dn;
-    a.gs = (fmt == QFMT_INT8_ROW || fmt == QFMT_INT4_ROW) ? 0 : g_up;   // per-row formats: one scale per row
+    a.gs = (fmt == QFMT_INT8_ROW || fmt == QFMT_INT4_ROW) ? 0 : gs_up;   // per-row formats: one scale per row
+    a.E = E; a.D = D; a.F = F; a.s = s; a.k = k;
+    const int up_rows = rows_per_launch(fmt, 2, D), down_rows = rows_per_launch(fmt, 1, F);
+    a.smax = up_rows < down_rows ? up_rows : down_rows;
+    if (a.smax > kExpertSmax) a.smax = kExpertSmax;
+    if (a.smax > s) a.smax = s;   // a batch holds pairs of distinct tokens unless a token repeats an id
+    if (a.smax < 1) return QSTATUS_BAD_DIM;
+    return QSTATUS_OK;
+}
+
+// Whether the call runs as the one fused launch (the plan fits and the
+// policy allows it).
+static bool expert_fuses(int fmt, const ExpertArgs& a)
+{
+    const int pol = kernel_policy();
+    if (!(pol == QKERNEL_AUTO || pol == QKERNEL_ROW) || (long long)a.s * a.k > kFusedMaxPairs) return false;
+    bool fits = false;
+    cudaError_t e = cudaSuccess;
+#define QG_CALL(name) expert_fused_##name(a, a.grid, nullptr, &fits, true)
+    QG_FMT_SWITCH(fmt, QG_CALL)
+#undef QG_CALL
+    return e == cudaSuccess && fits;
+}
+
+static int expert_group_impl(int fmt, int gs, const void* gate, const float* gate_s, const void* up,
+                             const float* up_s, const void* down, const float* down_s, int E, int D, int F,
+                             const float* x, int s, int k, const int32_t* ids, const float* wts, int act, float limit,
+                             float* out, void* workspace, size_t ws_bytes, int32_t* status_dev, void* stream,
+                             const FusedRoute* route)
+{
+    int g_up = 0, g_dn = 0;
+    int st = expert_checks(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids, wts, act, limit, out,
+                           workspace, ws_bytes, status_dev, &g_up, &g_dn);
+    if (st) return st;
+    ExpertArgs a;
+    st = expert_shape(fmt, g_up, E, D, F, s, k, a);
+    if (st) return st;
+    const int grid = a.grid;
+    a.act = act;
+    a.limit = limit;
     a.gate = gate; a.up = up; a.down = down;
     a.gate_s = gate_s; a.up_s = up_s; a.down_s = down_s;
-    a.E = E; a.D = D; a.F = F; a.s = s; a.k = k;
     a.x = x; a.ids = ids; a.wts = wts; a.out = out;
     a.ws = static_cast<unsigned char*>(workspace);
     a.status_dev = status_dev;
@@ -570,11 +598,6 @@ static int expert_group_impl(int fmt, int gs, const void* gate, const float* gat
         a.renorm = route->renorm;
         a.route_scale = route->scale;
     }
-    const int up_rows = rows_per_launch(fmt, 2, D), down_rows = rows_per_launch(fmt, 1, F);
-    a.smax = up_rows < down_rows ? up_rows : down_rows;
-    if (a.smax > kExpertSmax) a.smax = kExpertSmax;
-    if (a.smax > s) a.smax = s;   // a batch holds pairs of distinct tokens unless a token repeats an id
-    if (a.smax < 1) return QSTATUS_BAD_DIM;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
     cudaError_t e = cudaSuccess;
@@ -586,7 +609,7 @@ static int expert_group_impl(int fmt, int gs, const void* gate, const float* gat
             a.wait_ns = (unsigned long long)g_inject_ns.load();
         }
         bool launched = false;
-#define QG_CALL(name) expert_fused_##name(a, grid, cs, &launched)
+#define QG_CALL(name) expert_fused_##name(a, grid, cs, &launched, false)
         QG_FMT_SWITCH(fmt, QG_CALL)
 #undef QG_CALL
         if (launched || e != cudaSuccess) return launch_status(e);
@@ -650,6 +673,22 @@ int qexpert_group_routed(int fmt, int gs, const void* gate, const float* gate_s,
                         route_scale};
     return expert_group_impl(fmt, gs, gate, gate_s, up, up_s, down, down_s, E, D, F, x, s, k, ids_out, wts_out, act,
                              limit, out, workspace, ws_bytes, status_dev, stream, &fr);
+}
+
+int qexpert_group_launches(int fmt, int gs, int E, int D, int F, int s, int k, int routed)
+{
+    int g_up = 0, g_dn = 0;
+    int st = check_fmt(fmt, gs, D, &g_up);
+    if (st) return st;
+    st = check_fmt(fmt, gs, F, &g_dn);
+    if (st) return st;
+    if (E < 1 || D < 1 || F < 1 || s < 1 || k < 1 || D > kMaxI || F > kMaxI) return QSTATUS_BAD_DIM;
+    if ((long long)s * k > kMaxPairs) return QSTATUS_BAD_DIM;
+    ExpertArgs a;
+    st = expert_shape(fmt, g_up, E, D, F, s, k, a);
+    if (st) return st;
+    const int router = routed && E > kFusedRouteMaxE ? 1 : 0;   // the router kernel ahead of the group
+    return router + (expert_fuses(fmt, a) ? 1 : 4);
 }
 
 size_t qgemm_workspace(int I, int s)

@@ -527,11 +527,21 @@ __device__ __forceinline__ void stage_rows(float* xs, int xstride, const float* 
     }
 }
 
+// One float4 of activations; FRESH: through L2 only (written in this launch).
+template <bool FRESH>
+__device__ __forceinline__ float4 load_x4(const float* p)
+{
+    if constexpr (FRESH) return __ldcg(reinterpret_cast<const float4*>(p));
+    else return *reinterpret_cast<const float4*>(p);
+}
+
 // The same rows in the lane-interleaved layout, rows of xstride floats (a
 // multiple of 32 * EPL) zero beyond I: element i of chunk q = i / EPL (lane
 // l = q % 32 of warp step k = q / 32), quad j of the chunk, goes to float4
 // (k * EPL / 4 + j) * 32 + l.  Threads t of [0, nthreads) take part.
-template <int EPL>
+// FRESH: the rows were written earlier in the same launch (by other CTAs):
+// read them through L2 only.
+template <int EPL, bool FRESH = false>
 __device__ __forceinline__ void stage_rows_perm(float* xs, int xstride, const float* const* src, int nrows, int I,
                                                 int t, int nthreads)
 {
@@ -551,7 +561,7 @@ __device__ __forceinline__ void stage_rows_perm(float* xs, int xstride, const fl
 #pragma unroll 4
             for (int j = 0; j < QPC; j++) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (q * QPC + j < iq) v = *reinterpret_cast<const float4*>(src_q + 4 * j);
+                if (q * QPC + j < iq) v = load_x4<FRESH>(src_q + 4 * j);
                 *reinterpret_cast<float4*>(dst + 4 * 32 * j) = v;
             }
         }
@@ -563,7 +573,7 @@ __device__ __forceinline__ void stage_rows_perm(float* xs, int xstride, const fl
         const int s = idx / nq;
         const int qd = idx - s * nq;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (qd < iq) v = *reinterpret_cast<const float4*>(src[s] + 4 * qd);
+        if (qd < iq) v = load_x4<FRESH>(src[s] + 4 * qd);
         const int q = qd / QPC, j = qd - q * QPC;
         const int phys = ((q >> 5) * QPC + j) * 32 + (q & 31);
         *reinterpret_cast<float4*>(xs + (long long)s * xstride + 4 * phys) = v;

@@ -127,6 +127,12 @@ struct TileSource {
     TileLayout tile;
     CUtensorMap tm[3 * NM];
     long long row_mul[3], row_add[3];
+    // Activation rows come from before the launch.
+    static constexpr bool kFreshX = false;
+    __device__ const TileLayout& layout() const { return tile; }
+    __device__ const CUtensorMap* tmap(int i) const { return &tm[i]; }
+    __device__ long long rmul(int p) const { return row_mul[p]; }
+    __device__ long long radd(int p) const { return row_add[p]; }
 };
 
 template <int NM>
@@ -740,7 +746,7 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
     });
 }
 
-cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st, bool* launched)
+cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaStream_t st, bool* launched, bool dry)
 {
     *launched = false;
     const int gs_up = SK == SK_ROW ? a.D : a.gs, gs_dn = SK == SK_ROW ? a.F : a.gs;
@@ -748,18 +754,42 @@ cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaSt
     job.gate0 = to_mat(HostMat{a.gate, a.gate_s, a.F, a.D, gs_up});
     job.up0 = to_mat(HostMat{a.up, a.up_s, a.F, a.D, gs_up});
     job.down0 = to_mat(HostMat{a.down, a.down_s, a.D, a.F, gs_dn});
-    if (!plan_moe(a.D, a.F, job.gate0.gsh, job.down0.gsh, job.plan)) return cudaSuccess;
+    if (!plan_moe(a.D, a.F, gs_up, gs_dn, a.smax, job)) return cudaSuccess;
     const long long D = a.D, F = a.F;
-    job.rbA = code_row_bytes(a.D);
-    job.rbA_B = FMT == FMT_INT3_G64 ? D / 8 : 0;
-    job.sbA = SK == SK_ROW ? 0 : (SK == SK_E8M0 ? job.gate0.ngrp : 4ll * job.gate0.ngrp);
-    job.rbB = code_row_bytes(a.F);
-    job.rbB_B = FMT == FMT_INT3_G64 ? F / 8 : 0;
-    job.sbB = SK == SK_ROW ? 0 : (SK == SK_E8M0 ? job.down0.ngrp : 4ll * job.down0.ngrp);
-    job.up_bytes = F * job.rbA + F * job.rbA_B;
-    job.dn_bytes = D * job.rbB + D * job.rbB_B;
-    job.up_scales = F * job.gate0.ngrp;
-    job.dn_scales = D * job.down0.ngrp;
+    job.up_bytes = FMT == FMT_INT8_ROW ? F * D : FMT == FMT_INT3_G64 ? F * D / 4 + F * D / 8 : F * D / 2;
+    job.dn_bytes = FMT == FMT_INT8_ROW ? D * F : FMT == FMT_INT3_G64 ? D * F / 4 + D * F / 8 : D * F / 2;
+    job.up_scales = F * (D / gs_up);
+    job.dn_scales = D * (F / gs_dn);
+    {
+        constexpr int RA = TilePhase<2, kExpertSmax, MoeUpView>::R;
+        constexpr int RB = TilePhase<1, kExpertSmax, MoeDownView>::R;
+        TileSource<2> sa;
+        TileSource<1> sb;
+        sa.tile = job.la;
+        sb.tile = job.lb;
+        const void* wa[2] = {a.gate, a.up};
+        const float* sca[2] = {a.gate_s, a.up_s};
+        const void* wb[1] = {a.down};
+        const float* scb[1] = {a.down_s};
+        if ((long long)a.s * a.k * ((F + RA - 1) / RA) >= (1ll << 31) ||
+            (long long)a.s * a.k * ((D + RB - 1) / RB) >= (1ll << 31))
+            return cudaSuccess;
+        if (dry) {                                 // the plan only: it would launch
+            *launched = true;
+            return cudaSuccess;
+        }
+        if (!tile_sources<2>(sa, wa, sca, a.E, a.F, a.D, gs_up, job.up_bytes, RA) ||
+            !tile_sources<1>(sb, wb, scb, a.E, a.D, a.F, gs_dn, job.dn_bytes, RB))
+            return cudaSuccess;
+        for (int i = 0; i < 6; i++) job.tma[i] = sa.tm[i];
+        for (int i = 0; i < 3; i++) job.tmb[i] = sb.tm[i];
+        for (int p = 0; p < 3; p++) {
+            job.rmA[p] = sa.row_mul[p];
+            job.raA[p] = sa.row_add[p];
+            job.rmB[p] = sb.row_mul[p];
+            job.raB[p] = sb.row_add[p];
+        }
+    }
     const WsLayout L = ws_layout(a.D, a.F, a.s, a.k);
     job.x = a.x;
     job.ids = a.ids;
@@ -775,6 +805,7 @@ cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaSt
     job.s = a.s;
     job.k = a.k;
     job.P = a.s * a.k;
+    job.smax = a.smax;
     job.act = a.act;
     job.limit = a.limit;
     job.wait_ns = a.wait_ns;
@@ -784,11 +815,12 @@ cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaSt
     job.bias = a.bias;
     job.renorm = a.renorm;
     job.route_scale = a.route_scale;
+    const size_t smem = (size_t)job.la.total;
     static int granted[64];
-    cudaError_t e = set_smem(k_moe<FMT>, (size_t)job.plan.total, granted);
+    cudaError_t e = set_smem(k_moe<FMT>, smem, granted);
     if (e != cudaSuccess) return e;
     *launched = true;
-    return launch_pdl(k_moe<FMT>, dim3(grid), dim3(kMoeThreads), (size_t)job.plan.total, st, job);
+    return launch_pdl(k_moe<FMT>, dim3(grid), dim3(kTileThreads), smem, st, job);
 }
 
 int QG_CAT(device_error_, QG_NAME)(int clear)

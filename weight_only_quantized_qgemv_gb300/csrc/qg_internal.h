@@ -181,7 +181,8 @@ cudaError_t route_launch(int kind, const float* logits, const float* bias, int s
                                long long ldh, int act, float limit, int grid, cudaStream_t st);        \
     cudaError_t expert_up_##name(const ExpertArgs& a, int grid, cudaStream_t st);                       \
     cudaError_t expert_down_##name(const ExpertArgs& a, int grid, cudaStream_t st);                     \
-    cudaError_t expert_fused_##name(const ExpertArgs& a, int grid, cudaStream_t st, bool* launched);    \
+    cudaError_t expert_fused_##name(const ExpertArgs& a, int grid, cudaStream_t st, bool* launched,    \
+                                   bool dry);                                                      \
     cudaError_t dequant_##name(const HostMat& m, float* out, cudaStream_t st);                         \
     cudaError_t gemm_##name(const HostMat& m, const GemmArgs& g, cudaStream_t st);                     \
     size_t ring_bytes_##name(int nm);                                                                 \
