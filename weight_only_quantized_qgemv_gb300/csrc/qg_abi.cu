@@ -525,6 +525,12 @@ static int expert_checks(int fmt, int gs, const void* gate, const float* gate_s,
     return QSTATUS_OK;
 }
 
+// Pairs per expert batch at most (a batch's weights are streamed once for all
+// its pairs; each pair of a batch holds its own accumulators in the kernels).
+#ifndef QG_SMAX_CAP
+#define QG_SMAX_CAP kExpertSmax
+#endif
+
 // The launch shape of an expert group (no pointers): the grid, the batch
 // size smax and the tile counts of the four-launch path.
 static int expert_shape(int fmt, int gs_up, int E, int D, int F, int s, int k, ExpertArgs& a)
@@ -550,7 +556,7 @@ static int expert_shape(int fmt, int gs_up, int E, int D, int F, int s, int k, E
     a.E = E; a.D = D; a.F = F; a.s = s; a.k = k;
     const int up_rows = rows_per_launch(fmt, 2, D), down_rows = rows_per_launch(fmt, 1, F);
     a.smax = up_rows < down_rows ? up_rows : down_rows;
-    if (a.smax > kExpertSmax) a.smax = kExpertSmax;
+    if (a.smax > QG_SMAX_CAP) a.smax = QG_SMAX_CAP;
     if (a.smax > s) a.smax = s;   // a batch holds pairs of distinct tokens unless a token repeats an id
     if (a.smax < 1) return QSTATUS_BAD_DIM;
     return QSTATUS_OK;

@@ -491,6 +491,7 @@ static bool plan_tile(int NM, int R, int I, int gs, int xrows, TileLayout& L)
     if (P > QG_TILE_PMAX) P = QG_TILE_PMAX;
     if (P < 2) return false;
     L.P = P;
+    L.warp_bytes = P * L.slot_bytes;
     L.bar_off = L.ring_off + P * per_p;
     L.total = L.bar_off + 8 * (kTileWarps * P + 1);
     return true;
@@ -695,7 +696,11 @@ cudaError_t QG_CAT(expert_up_, QG_NAME)(const ExpertArgs& a, int grid, cudaStrea
         if (kernel_policy() != QKERNEL_RING && (long long)a.s * a.k * ((a.F + R - 1) / R) < (1ll << 31) &&
             plan_tile(2, R, a.D, gs, a.smax, job.tile) &&
             tile_sources<2>(job, w, sc, a.E, a.F, a.D, gs, job.mat_bytes, R))
+        {
+            if (a.smax <= 1) return launch_tile<2, 1>(job, grid, st);
+            if (a.smax <= 2) return launch_tile<2, 2>(job, grid, st);
             return launch_tile<2, kExpertSmax>(job, grid, st);
+        }
     }
     return with_share(job.gate0.gsh, [&](auto sh) -> cudaError_t {
         auto kern = k_stream<2, kExpertSmax, ExpertUpJob, 0, decltype(sh)::value>;
@@ -734,7 +739,11 @@ cudaError_t QG_CAT(expert_down_, QG_NAME)(const ExpertArgs& a, int grid, cudaStr
         if (kernel_policy() != QKERNEL_RING && (long long)a.s * a.k * ((a.D + R - 1) / R) < (1ll << 31) &&
             plan_tile(1, R, a.F, gs, a.smax, job.tile) &&
             tile_sources<1>(job, w, sc, a.E, a.D, a.F, gs, job.mat_bytes, R))
+        {
+            if (a.smax <= 1) return launch_tile<1, 1>(job, grid, st);
+            if (a.smax <= 2) return launch_tile<1, 2>(job, grid, st);
             return launch_tile<1, kExpertSmax>(job, grid, st);
+        }
     }
     return with_share(job.down0.gsh, [&](auto sh) -> cudaError_t {
         auto kern = k_stream<1, kExpertSmax, ExpertDownJob, 0, decltype(sh)::value>;
@@ -761,8 +770,8 @@ cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaSt
     job.up_scales = F * (D / gs_up);
     job.dn_scales = D * (F / gs_dn);
     {
-        constexpr int RA = TilePhase<2, kExpertSmax, MoeUpView>::R;
-        constexpr int RB = TilePhase<1, kExpertSmax, MoeDownView>::R;
+        constexpr int RA = TilePhase<2, 1, MoeUpView>::R;
+        constexpr int RB = TilePhase<1, 1, MoeDownView>::R;
         TileSource<2> sa;
         TileSource<1> sb;
         sa.tile = job.la;
@@ -815,12 +824,8 @@ cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaSt
     job.bias = a.bias;
     job.renorm = a.renorm;
     job.route_scale = a.route_scale;
-    const size_t smem = (size_t)job.la.total;
-    static int granted[64];
-    cudaError_t e = set_smem(k_moe<FMT>, smem, granted);
-    if (e != cudaSuccess) return e;
     *launched = true;
-    return launch_pdl(k_moe<FMT>, dim3(grid), dim3(kTileThreads), smem, st, job);
+    return launch_moe(job, grid, st);
 }
 
 int QG_CAT(device_error_, QG_NAME)(int clear)

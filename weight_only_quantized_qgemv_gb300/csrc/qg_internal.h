@@ -112,6 +112,7 @@ struct TileLayout {
     int slot_bytes;    // slot stride
     int tx_bytes;      // bytes the tensor copies of one slot deliver
     int ring_off;      // first ring
+    int warp_bytes;    // ring stride from one warp to the next (>= P * slot_bytes)
     int bar_off;       // P full barriers per warp, then the CTA barrier
     int total;         // dynamic shared memory of the launch
     int nslices;       // slices per row

@@ -177,13 +177,15 @@ __device__ __forceinline__ int moe_bound(const int* first, int nb, int P, int tp
     return (int)((long long)lo * tpb + (x - (long long)first[lo] * tpb) / n);
 }
 
-template <int F_>
+// SM: the most pairs a batch holds (job.smax <= SM): the passes keep SM
+// accumulator sets, so a launch whose batches hold one pair carries one.
+template <int F_, int SM>
 __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__ MoeJob job)
 {
     static_assert(F_ == FMT, "one format per translation unit");
     constexpr int NT = kTileThreads;
-    using PhaseA = TilePhase<2, kExpertSmax, MoeUpView>;
-    using PhaseB = TilePhase<1, kExpertSmax, MoeDownView>;
+    using PhaseA = TilePhase<2, SM, MoeUpView>;
+    using PhaseB = TilePhase<1, SM, MoeDownView>;
     const int tid = threadIdx.x, lane = tid & 31;
     const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
     const uint32_t sbase = smem_base();
@@ -301,26 +303,29 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
     float* xs = reinterpret_cast<float*>(qg_smem4);
 
     // ---- phase A: gate and up rows, h = act(g, u) ----
+    PhaseA::init_barriers(job.la, sbase, warp);    // both passes' barriers (separate words)
+    PhaseB::init_barriers(job.lb, sbase, warp);
+    __syncthreads();
     {
         const MoeUpView up{job, s_bt, s_tok, job.act, job.limit};
         PhaseA pa(up, sbase, warp, a0, a1, tpbA);
-        __syncthreads();                           // the ring barriers are initialized
         pa.prime();
         if (!pa.run(xs)) {
             pa.drain();
             s_misc[3] = 1;                         // a wait of this CTA ran out
         }
     }
-    __syncthreads();                               // every warp is done with phase A's rings and staged rows
+    // The warp's ring is idle now (every phase A slice it issued was
+    // consumed), and each warp's ring region is the same in both passes: it
+    // issues its first down slices at once, while the barrier waits.
     const MoeDownView dn{job, s_bt, job.act, job.limit};
     PhaseB pb(dn, sbase, warp, b0, b1, tpbB);
-    __syncthreads();
-    pb.prime();                                    // the down rows stream in while the barrier waits
+    pb.prime();
 
     // ---- grid barrier: every CTA's h rows written ----
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
+        __threadfence();                           // the CTA's h stores (ordered before by the barrier)
         if (!(job.withhold && c == 0)) atomicAdd(&job.ctr[0], 1u);
         if (!wait_count(&job.ctr[0], (unsigned)G, job.wait_ns)) s_misc[2] = 0;
         __threadfence();
@@ -343,9 +348,9 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
     }
 
     // ---- second barrier: every z row written; then the rank-order sums ----
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
+        __threadfence();
         atomicAdd(&job.ctr[1], 1u);
         if (!wait_count(&job.ctr[1], (unsigned)G, job.wait_ns)) {
             moe_fail(job.ctr);
@@ -391,6 +396,25 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
 #define QG_MOE 1
 #endif
 
+// Launches k_moe<FMT, SM> (its own record of the shared memory granted).
+template <int SM>
+static cudaError_t launch_moe_sm(const MoeJob& job, int grid, cudaStream_t st)
+{
+    const size_t smem = (size_t)job.la.total;
+    static int granted[64];
+    cudaError_t e = set_smem(k_moe<FMT, SM>, smem, granted);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_moe<FMT, SM>, dim3(grid), dim3(kTileThreads), smem, st, job);
+}
+
+// Launches k_moe with the fewest accumulator sets that hold job.smax pairs.
+static cudaError_t launch_moe(const MoeJob& job, int grid, cudaStream_t st)
+{
+    if (job.smax <= 1) return launch_moe_sm<1>(job, grid, st);
+    if (job.smax <= 2) return launch_moe_sm<2>(job, grid, st);
+    return launch_moe_sm<kExpertSmax>(job, grid, st);
+}
+
 // Plans the fused launch's shared memory: the staged activation rows (smax
 // rows of max(D, F) inputs), one ring region that phase A's and then phase
 // B's slots share, each phase's barriers, the pair tables.  False when the
@@ -398,8 +422,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
 static bool plan_moe(int D, int F, int gs_up, int gs_dn, int smax, MoeJob& j)
 {
     if (!QG_MOE) return false;
-    constexpr int RA = TilePhase<2, kExpertSmax, MoeUpView>::R;
-    constexpr int RB = TilePhase<1, kExpertSmax, MoeDownView>::R;
+    constexpr int RA = TilePhase<2, 1, MoeUpView>::R;     // (one-pair passes: the height does not depend on SM)
+    constexpr int RB = TilePhase<1, 1, MoeDownView>::R;
     if (!plan_tile(2, RA, D, gs_up, smax, j.la) || !plan_tile(1, RB, F, gs_dn, smax, j.lb)) return false;
     const int NW = kTileWarps;
     const int ring_off = j.la.ring_off > j.lb.ring_off ? j.la.ring_off : j.lb.ring_off;
@@ -412,6 +436,7 @@ static bool plan_moe(int D, int F, int gs_up, int gs_dn, int smax, MoeJob& j)
     const int ring = NW * (PA * j.la.slot_bytes > PB * j.lb.slot_bytes ? PA * j.la.slot_bytes : PB * j.lb.slot_bytes);
     j.la.P = PA;
     j.lb.P = PB;
+    j.la.warp_bytes = j.lb.warp_bytes = ring / NW;   // a warp's region is the same in both passes
     j.la.ring_off = j.lb.ring_off = ring_off;
     j.la.bar_off = ring_off + ring;
     j.lb.bar_off = j.la.bar_off + 8 * (NW * PA + 1);

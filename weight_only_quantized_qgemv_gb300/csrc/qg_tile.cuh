@@ -105,10 +105,20 @@ struct TilePhase {
     int slot;
     uint32_t so, phase;
 
-    // The pass over tiles [t0_, t1_) of tpb_ tiles per batch; lane 0 of each
-    // warp initializes the warp's slot barriers and thread 0 the CTA barrier.
-    // The caller makes the initialization visible to the CTA (__syncthreads)
-    // before any other call.
+    // Lane 0 of each warp initializes the warp's slot barriers of layout L,
+    // thread 0 the CTA barrier; the caller makes that visible to the CTA
+    // (__syncthreads) before the pass's first call.
+    static __device__ __forceinline__ void init_barriers(const TileLayout& L, uint32_t sbase_, int warp_)
+    {
+        const uint32_t f0 = sbase_ + (uint32_t)L.bar_off + 8u * (uint32_t)(warp_ * L.P);
+        if ((threadIdx.x & 31) == 0)
+            for (int p = 0; p < L.P; p++) mbar_init(f0 + 8u * p, 1);
+        if (threadIdx.x == 0) mbar_init(sbase_ + (uint32_t)L.bar_off + 8u * (uint32_t)(NW * L.P), NW * 32);
+        mbar_init_fence();
+    }
+
+    // The pass over tiles [t0_, t1_) of tpb_ tiles per batch (its barriers
+    // initialized).
     __device__ __forceinline__ TilePhase(const Job& j, uint32_t sbase_, int warp_, int t0_, int t1_, int tpb_)
         : job(j)
     {
@@ -133,14 +143,10 @@ struct TilePhase {
         sbase = sbase_;
         full0 = sbase + (uint32_t)L.bar_off + 8u * (uint32_t)(warp * P);
         ctabar = sbase + (uint32_t)L.bar_off + 8u * (uint32_t)(NW * P);
-        ring0 = (uint32_t)L.ring_off + (uint32_t)warp * (uint32_t)P * slot_bytes;
+        ring0 = (uint32_t)L.ring_off + (uint32_t)warp * (uint32_t)L.warp_bytes;
         t0 = t0_;
         t1 = t1_;
         tpb = tpb_;
-        if (leader)
-            for (int p = 0; p < P; p++) mbar_init(full0 + 8u * p, 1);
-        if (threadIdx.x == 0) mbar_init(ctabar, NW * 32);
-        mbar_init_fence();
         pk = 0;
         pb = -1;
         pe = 0;
@@ -366,9 +372,10 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_tile(const __grid_constant_
     const long long T = (long long)job.nbatch() * tpb;
     int t0, t1;
     job.cta_tiles(blockIdx.x, gridDim.x, T, t0, t1);
-    TilePhase<NM, S, Job> ph(job, sbase, warp, t0, t1, tpb);
+    TilePhase<NM, S, Job>::init_barriers(job.layout(), sbase, warp);
     __syncthreads();
     if (t0 >= t1) return;
+    TilePhase<NM, S, Job> ph(job, sbase, warp, t0, t1, tpb);
     ph.prime();
     if (!ph.run(reinterpret_cast<float*>(qg_smem4))) {
         tile_fail(status);
