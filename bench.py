@@ -20,6 +20,7 @@ samples of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import glob
 import hashlib
 import json
@@ -293,9 +294,12 @@ class ExpertBench:
         self.gs = wl.gs if wl.fmt in GROUPED else 0
         self.expert_bytes = wl.expert_bytes()
         self.route_bytes = [len(np.unique(self.ids_host[r])) * self.expert_bytes for r in range(self.nroutes)]
-        # one persistent launch up to 256 (token, rank) pairs, else prep, gate/up, down, combine
-        self.fused = wl.s * wl.k <= 256
-        self.launches_per_step = 1 if self.fused else 4
+        # the library says how many launches a call makes: one persistent
+        # launch up to 256 (token, rank) pairs, else prep, gate/up, down, combine
+        from weight_only_quantized_qgemv_gb300 import qexpert_group_launches
+        self.launches_per_step = qexpert_group_launches(wl.fmt, self.gs, wl.E, wl.D, wl.F, wl.s, wl.k,
+                                                        routed=device_route)
+        self.fused = self.launches_per_step == 1
         self.device_route = device_route
         if device_route:
             # routing on the device from seeded logits: softmax top-k, renormalized
@@ -305,8 +309,6 @@ class ExpertBench:
             self.wts_out = torch.empty(wl.s, wl.k, dtype=torch.float32, device=device)
             top = np.argpartition(-self.logits_host, wl.k - 1, axis=2)[:, :, :wl.k]
             self.route_bytes = [len(np.unique(top[r])) * self.expert_bytes for r in range(self.nroutes)]
-            if wl.E > 256:                                     # a router launch of its own ahead
-                self.launches_per_step += 1
 
     def _call(self, r, x, ids, wts, stream, logits=None):
         from weight_only_quantized_qgemv_gb300 import QROUTE_SOFTMAX, qexpert_group_act, qexpert_group_routed
@@ -606,9 +608,9 @@ def gemv_kernel_name(wl, sms=152):
     return "k_tile" if (shares and fits and not short) else "k_stream"
 
 
-def expert_kernel_name(wl):
+def expert_kernel_name(bench):
     """The launches one qexpert_group call of this workload runs."""
-    if wl.s * wl.k <= 256:
+    if bench.fused:
         return "k_moe (the whole expert group in one launch)"
     return "whole qexpert_group call (k_expert_prep + k_tile gate/up + k_tile down + k_expert_combine)"
 
@@ -644,7 +646,7 @@ def est_call_seconds(wl):
 def kernel_name(bench):
     if isinstance(bench, GemvBench):
         return gemv_kernel_name(bench.wl)
-    return expert_kernel_name(bench.wl)
+    return expert_kernel_name(bench)
 
 
 def workload_line(name, args, device, l2, stream, torch, peak, e2e_steps=200):
@@ -700,8 +702,16 @@ def main():
                     help="expert workloads: route on the device from seeded router logits (qexpert_group_routed)")
     ap.add_argument("--swiglu-limit", type=float, default=None,
                     help="expert workloads: clamped SwiGLU with this limit instead of SwiGLU")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="expert workloads, for profiler captures: a store of this many experts instead of the "
+                         "workload's (each call still routes every token to k distinct experts, so a call's "
+                         "work is unchanged; the store, and so the device memory, shrinks)")
     args = ap.parse_args()
     wl = synth.workload(args.workload)
+    if args.experts is not None:
+        if not isinstance(wl, synth.ExpertWorkload) or not (wl.k <= args.experts <= wl.E):
+            raise SystemExit("--experts applies to expert workloads, between k and the workload's E")
+        wl = dataclasses.replace(wl, E=args.experts, _cache={})
     world, rank, local = dist_env()
     args.steps = max(1, args.steps)
     args.warmup = max(3, args.warmup)

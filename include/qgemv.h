@@ -150,8 +150,9 @@ int qgate_up_act(int fmt, int gs, const void* wg, const float* sg,
 
 /* Bytes of workspace qexpert_group needs for these sizes.  The workspace
  * must hold zeros before its first use (cudaMemset it once after allocating
- * it); every call leaves it that way -- its first words are the counters of
- * the one-launch expert group's grid barriers. */
+ * it); every call leaves the words that must be zero that way -- its first
+ * words are the one-launch expert group's counters (per-batch readiness and
+ * its closing barrier). */
 size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
 
 /*
@@ -173,8 +174,10 @@ size_t qexpert_group_workspace(int E, int D, int F, int s, int k);
  *             the launch ran out.  The host-side return cannot see device-side
  *             checks.
  * Up to 256 (token, rank) pairs the call is one persistent launch (gate/up,
- * act, down and the rank-order sum; its CTAs, one per SM, meet at two grid
- * barriers, so the launch needs every SM of the device at once); past that,
+ * act, down and the rank-order sum; its CTAs, one per SM, wait on one another
+ * -- the down rows of an expert batch for that batch's gate/up rows, the sums
+ * for every down row -- so the launch needs every SM of the device at once;
+ * qexpert_group_launches tells which path a call takes); past that,
  * and under QKERNEL_RING or QKERNEL_TILE, four launches that stream each
  * expert's weights once for all the pairs routed to it.  Repeated ids in a row
  * are allowed and summed.  s * k <= 4096.
@@ -328,8 +331,9 @@ int qexpert_group_routed(int fmt, int gs,
  * Test hook (no counterpart in the pages, whose backends inject their faults
  * through environment switches): arms one fault for the next one-launch
  * expert group of this process.  QDEBUG_WITHHOLD_SIGNAL makes one CTA of that
- * launch skip its phase-A arrival, so the other CTAs' bounded waits run out
- * after wait_ns nanoseconds: the launch records QSTATUS_DEVICE_TIMEOUT (in
+ * launch skip counting its finished gate/up rows, so the waits of the CTAs
+ * that need them run out after wait_ns nanoseconds (every wait of that launch
+ * is bounded by wait_ns): the launch records QSTATUS_DEVICE_TIMEOUT (in
  * qdevice_error and in the call's status word), its results are undefined, it
  * returns, and it leaves the workspace ready for the next call.  Nothing
  * faults or waits without bound.  QDEBUG_NONE disarms.  Returns QSTATUS_OK,

@@ -730,12 +730,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
         if ((n & 15u) == 0 && global_ns() - t0 > kWaitNs) return false;   // the clock every 16 tries
     }
 }
-// Every thread of the CTA arrives on `bar` (initialized for all of them) and
-// waits for the others; `parity` tracks the barrier's phase.  False after
-// kWaitNs.
+// Every warp of the CTA arrives on `bar` (initialized for one arrival per
+// warp: lane 0 arrives once the warp's lanes have met at __syncwarp, which
+// orders their memory operations before the arrival) and every thread waits
+// for the others; `parity` tracks the barrier's phase.  False after kWaitNs.
+// One arrival per warp rather than per thread keeps the barrier's
+// shared-memory updates to one per warp.
 __device__ __forceinline__ bool cta_barrier(uint32_t bar, uint32_t& parity)
 {
-    mbar_arrive(bar);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
     const bool ok = mbar_wait(bar, parity);
     parity ^= 1u;
     return ok;

@@ -127,8 +127,13 @@ struct TileSource {
     TileLayout tile;
     CUtensorMap tm[3 * NM];
     long long row_mul[3], row_add[3];
-    // Activation rows come from before the launch.
+    // Activation rows come from before the launch; no per-batch signals.
     static constexpr bool kFreshX = false;
+    static constexpr bool kSignals = false;
+    static constexpr bool kWaits = false;
+    __device__ void warp_done(int, int) const {}
+    __device__ void segment_poll(int) const {}
+    __device__ bool segment_ready() const { return true; }
     __device__ const TileLayout& layout() const { return tile; }
     __device__ const CUtensorMap* tmap(int i) const { return &tm[i]; }
     __device__ long long rmul(int p) const { return row_mul[p]; }
@@ -807,6 +812,7 @@ cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaSt
     job.h = reinterpret_cast<float*>(a.ws + L.h);
     job.z = reinterpret_cast<float*>(a.ws + L.z);
     job.ctr = reinterpret_cast<unsigned*>(a.ws + L.hdr) + 4;
+    job.done = reinterpret_cast<unsigned*>(a.ws + L.done);
     job.status = a.status_dev;
     job.E = a.E;
     job.D = a.D;

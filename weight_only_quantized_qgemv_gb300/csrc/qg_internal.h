@@ -36,7 +36,9 @@ struct HostMat {
 };
 
 // Workspace of qexpert_group (all offsets 256-byte aligned):
-//   hdr      int32[8]     [0] status, [1] batches, [2] pairs
+//   hdr      int32[8]     [0] status, [1] batches, [2] pairs (four-launch path);
+//                         [4..7] the one-launch path's counters (zero between calls)
+//   done     int32[256]   one-launch path: phase-A row tiles finished per batch (zero between calls)
 //   batches  int4[P]      (expert, first sorted pair, pairs in batch, 0)
 //   pair_tok int32[P]     token of the sorted pair
 //   pair_of  int32[P]     sorted position of pair t * k + r
@@ -45,7 +47,7 @@ struct HostMat {
 //   z        f32[P][D]    down h of each sorted pair
 constexpr int kMaxGrid = 1024;              // CTAs of an expert launch
 struct WsLayout {
-    size_t hdr, batches, pair_tok, pair_of, bounds, h, z, total;
+    size_t hdr, done, batches, pair_tok, pair_of, bounds, h, z, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -57,6 +59,7 @@ inline WsLayout ws_layout(int D, int F, int s, int k)
     WsLayout L;
     size_t off = 0;
     L.hdr = off;      off = align256(off + 8 * sizeof(int32_t));
+    L.done = off;     off = align256(off + 256 * sizeof(int32_t));
     L.batches = off;  off = align256(off + P * 4 * sizeof(int32_t));
     L.pair_tok = off; off = align256(off + P * sizeof(int32_t));
     L.pair_of = off;  off = align256(off + P * sizeof(int32_t));

@@ -17,20 +17,23 @@
 //  * phase A: the tile kernel's streaming pass over the gate and up rows of
 //    the batches -- every warp streams its own row tiles through a ring of
 //    tensor copies, the batch's activation rows staged once per CTA in shared
-//    memory -- storing h = act(g, u) per (pair, row) in the workspace;
-//  * the down rows' first slices are issued into the rings, then a grid
-//    barrier: each CTA adds one to a counter once its h rows are written and
-//    waits (bounded) until every CTA has -- the copies land meanwhile;
-//  * phase B: the same pass over the down rows against the pairs' h rows
-//    (staged from L2), storing z = down h per (pair, row);
+//    memory -- storing h = act(g, u) per (pair, row) in the workspace; each
+//    warp then adds the number of row tiles it finished to its batch's
+//    counter (a release reduction);
+//  * each warp issues its first down-row slices into its ring as soon as its
+//    phase-A slices are consumed (the down weights do not depend on h);
+//  * phase B: the same pass over the down rows against the pairs' h rows,
+//    staged from L2 once the batch's counter holds all its phase-A tiles
+//    (thread 0 waits, bounded; a CTA thus waits only for the warps that
+//    computed the batches it needs), storing z = down h per (pair, row);
 //  * a second barrier, then each CTA sums its share of the output columns in
 //    rank order, out[t][d] = sum_r w[t][r] z[pair(t, r)][d], and the last CTA
 //    to finish clears the counters (the workspace holds zeros before the
 //    first call and after every call).
 // The passes are the tile kernel's own, so every h, z and out value has the
 // bits of the four-launch path.  Every wait is bounded; one that runs out
-// records QSTATUS_DEVICE_TIMEOUT, and the CTA still arrives at every later
-// counter so the others finish and the counters are cleared.
+// records QSTATUS_DEVICE_TIMEOUT, and the CTA still arrives at the closing
+// counters so the others finish and the counters are cleared.
 #pragma once
 
 constexpr int kMoeMaxPairs = 256;               // s * k of the fused launch
@@ -54,15 +57,15 @@ struct MoeJob {
     float* out;                     // [s][D]
     float* h;                       // workspace [P][F], by sorted pair position
     float* z;                       // workspace [P][D]
-    unsigned* ctr;                  // workspace: [0] phase A arrivals, [1] phase B arrivals, [2] finished CTAs,
-                                    // [3] a wait ran out
+    unsigned* ctr;                  // workspace: [1] phase B arrivals, [2] finished CTAs, [3] a wait ran out
+    unsigned* done;                 // workspace: phase-A row tiles finished per batch
     int* status;                    // optional status word
     int E, D, F, s, k, P, smax;
     int tab_off;                    // shared offset of the pair tables
     int act;
     float limit;
     unsigned long long wait_ns;     // bound of every grid-barrier wait
-    int withhold;                   // test hook: CTA 0 does not signal phase A
+    int withhold;                   // test hook: CTA 0 does not count its phase-A tiles
     // routing inside the prologue (route_kind >= 0): ids / wts are its outputs
     int route_kind;
     const float* logits;
@@ -71,17 +74,49 @@ struct MoeJob {
     float route_scale;
 };
 
+// Waits until *c >= target (acquire); false after wait_ns.
+__device__ __forceinline__ bool wait_count(const unsigned* c, unsigned target, unsigned long long wait_ns)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= target) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t n = 1;; n++) {
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+        if (v >= target) return true;
+        if ((n & 15u) == 0 && global_ns() - t0 > wait_ns) return false;
+        __nanosleep(64);
+    }
+}
+
 // The two passes' views of the launch: batches and tokens from the prologue's
-// shared tables, tensor maps from the launch's parameters.
+// shared tables, tensor maps from the launch's parameters.  Phase A tells
+// each batch's counter how many of its row tiles a warp has finished (h rows
+// written); phase B stages a batch's h rows once its counter is complete, so
+// a CTA waits only for the warps that computed the batches it needs.
 struct MoeUpView {
     static constexpr bool kLoopS = true;       // one pass of arithmetic per pair of a batch
     static constexpr bool kWaitFirst = true;   // (the prologue waited)
     static constexpr bool kFreshX = false;     // x comes from before the launch
+    static constexpr bool kSignals = true;
+    static constexpr bool kWaits = false;
     const MoeJob& g;
     const int4* bt;                            // (expert, first sorted position, pairs, 0) per batch
     const int* tok;                            // token of each sorted position
     int act;
     float limit;
+    // the warp's h rows of batch b are stored: lane 0 publishes its tile count
+    // with a release reduction (after __syncwarp, the release covers every
+    // lane's stores; phase B reads the counter with acquire loads)
+    __device__ void warp_done(int b, int tiles) const
+    {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0 && !(g.withhold && blockIdx.x == 0))
+            asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(&g.done[b]), "r"((unsigned)tiles)
+                         : "memory");
+    }
+    __device__ void segment_poll(int) const {}
+    __device__ bool segment_ready() const { return true; }
     __device__ const TileLayout& layout() const { return g.la; }
     __device__ const CUtensorMap* tmap(int i) const { return &g.tma[i]; }
     __device__ long long rmul(int p) const { return g.rmA[p]; }
@@ -111,10 +146,22 @@ struct MoeDownView {
     static constexpr bool kLoopS = true;
     static constexpr bool kWaitFirst = true;
     static constexpr bool kFreshX = true;      // h was written by this launch's CTAs: read through L2
+    static constexpr bool kSignals = false;
+    static constexpr bool kWaits = true;
     const MoeJob& g;
     const int4* bt;
     int act;                                   // (unused: one matrix)
     float limit;
+    unsigned need;                             // phase-A row tiles per batch
+    int* flag;                                 // shared: the last wait's outcome
+    __device__ void warp_done(int, int) const {}
+    // thread 0 waits (bounded) until all of batch b's h rows are written (one
+    // poller per CTA keeps the counters' L2 line cool)
+    __device__ void segment_poll(int b) const
+    {
+        if (threadIdx.x == 0) *flag = wait_count(&g.done[b], need, g.wait_ns) ? 1 : 0;
+    }
+    __device__ bool segment_ready() const { return *flag != 0; }
     __device__ const TileLayout& layout() const { return g.lb; }
     __device__ const CUtensorMap* tmap(int i) const { return &g.tmb[i]; }
     __device__ long long rmul(int p) const { return g.rmB[p]; }
@@ -136,21 +183,6 @@ struct MoeDownView {
     }
     __device__ int width() const { return g.F; }
 };
-
-// Waits until *c >= target (acquire); false after wait_ns.
-__device__ __forceinline__ bool wait_count(const unsigned* c, unsigned target, unsigned long long wait_ns)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-    if (v >= target) return true;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t n = 1;; n++) {
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-        if (v >= target) return true;
-        if ((n & 15u) == 0 && global_ns() - t0 > wait_ns) return false;
-        __nanosleep(64);
-    }
-}
 
 // A wait of this launch ran out: the library's error word now, the call's
 // status word from the last CTA (through ctr[3]).
@@ -201,7 +233,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
     int* s_first = s_nstart + kMoeMaxPairs;            // [batch] first position; [nb] = P
     int4* s_bt = reinterpret_cast<int4*>(s_first + kMoeMaxPairs + 4);
     int* s_misc = reinterpret_cast<int*>(s_bt + kMoeMaxPairs);
-    // s_misc: [0] a bad id, [1] batches, [2] grid waits ok, [4..7] tile bounds, [16..32) starts per warp
+    // s_misc: [0] a bad id, [1] batches, [2] grid waits ok, [3] a wait of this CTA ran out, [4..7] tile
+    // bounds, [8] phase B's batch wait, [16..32) starts per warp
 
     pdl_wait_prev();                               // ids, weights, x and the workspace come from before
     pdl_allow_next();
@@ -317,23 +350,15 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
     }
     // The warp's ring is idle now (every phase A slice it issued was
     // consumed), and each warp's ring region is the same in both passes: it
-    // issues its first down slices at once, while the barrier waits.
-    const MoeDownView dn{job, s_bt, job.act, job.limit};
+    // issues its first down slices at once (the down weights do not depend
+    // on h); phase B then waits per batch for the h rows it stages.
+    const MoeDownView dn{job, s_bt, job.act, job.limit, (unsigned)tpbA, s_misc + 8};
     PhaseB pb(dn, sbase, warp, b0, b1, tpbB);
     pb.prime();
-
-    // ---- grid barrier: every CTA's h rows written ----
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();                           // the CTA's h stores (ordered before by the barrier)
-        if (!(job.withhold && c == 0)) atomicAdd(&job.ctr[0], 1u);
-        if (!wait_count(&job.ctr[0], (unsigned)G, job.wait_ns)) s_misc[2] = 0;
-        __threadfence();
-    }
-    __syncthreads();
+    __syncthreads();                               // every warp is done with phase A's staged x
 
     // ---- phase B: down rows, z = down h (all warps of the CTA, or none) ----
-    if (s_misc[2] != 0 && s_misc[3] == 0) {
+    if (s_misc[3] == 0) {
         if (!pb.run(xs)) {
             pb.drain();
             s_misc[3] = 1;
@@ -384,7 +409,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
         if (prev == (unsigned)G - 1) {
             const unsigned failed = atomicExch(&job.ctr[3], 0u);
             if (job.status) *job.status = failed ? QSTATUS_DEVICE_TIMEOUT : QSTATUS_OK;
-            job.ctr[0] = 0;
+            for (int b = 0; b < nb; b++) job.done[b] = 0;
             job.ctr[1] = 0;
             job.ctr[2] = 0;
             __threadfence();

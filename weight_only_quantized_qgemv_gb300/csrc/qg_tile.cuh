@@ -71,7 +71,11 @@ struct TileWalk {
 // producer (lane 0 issues, every lane keeps the same state) and its consumer.
 // The job supplies the slot layout (layout()), the tensor maps (tmap()), the
 // tensor rows of each piece (rmul(), radd()), its batches and where results
-// go.  A launch may run several passes one after another, each with its own
+// go; a job with kSignals also hears when a warp has stored its results of a
+// batch (warp_done(batch, tiles), every lane of the warp calling), and one
+// with kWaits holds each batch back until its activations are complete
+// (thread 0 waits in segment_poll(batch); every thread then reads
+// segment_ready()).  A launch may run several passes one after another, each with its own
 // ring barriers; a pass may prime its ring (issue its first P slices) long
 // before it consumes.
 template <int NM, int S, class Job>
@@ -113,7 +117,7 @@ struct TilePhase {
         const uint32_t f0 = sbase_ + (uint32_t)L.bar_off + 8u * (uint32_t)(warp_ * L.P);
         if ((threadIdx.x & 31) == 0)
             for (int p = 0; p < L.P; p++) mbar_init(f0 + 8u * p, 1);
-        if (threadIdx.x == 0) mbar_init(sbase_ + (uint32_t)L.bar_off + 8u * (uint32_t)(NW * L.P), NW * 32);
+        if (threadIdx.x == 0) mbar_init(sbase_ + (uint32_t)L.bar_off + 8u * (uint32_t)(NW * L.P), NW);
         mbar_init_fence();
     }
 
@@ -220,6 +224,12 @@ struct TilePhase {
             const int s_act = job.batch_S(b);
             // stage the batch's activation rows (after everyone is done with the last)
             if (seg0 != t0 && !cta_barrier(ctabar, cta_phase)) { ok = false; break; }
+            if constexpr (Job::kWaits) {
+                // one thread waits until the batch's activations are complete and
+                // posts the outcome; the CTA barrier hands it to every warp
+                job.segment_poll(b);
+                if (!cta_barrier(ctabar, cta_phase) || !job.segment_ready()) { ok = false; break; }
+            }
             if (!Job::kWaitFirst && seg0 == t0) pdl_wait_prev();   // before the first read of activations
             {
                 const float* src[S];
@@ -243,7 +253,8 @@ struct TilePhase {
                     for (int r = 0; r < R; r++) sso[m * R + r] = ls + m * s_step + (uint32_t)(r * sbox);
             }
             Sink<Job, S, R, NM> sink{job, b, s_act};
-            for (int t = seg0 + warp; ok && t < seg1; t += NW) {
+            int mine = 0;                             // tiles of the segment this warp finished
+            for (int t = seg0 + warp; ok && t < seg1; t += NW, mine++) {
                 const long long row0 = (long long)(t - b * tpb) * R;
                 float acc[S][NR];
 #pragma unroll
@@ -330,6 +341,9 @@ struct TilePhase {
                     const float red = warp_reduce_scatter<V>(v, lane);
                     sink.template put<V>(red, reduce_scatter_index<V>(lane), lane < V, row0, rows);
                 }
+            }
+            if constexpr (Job::kSignals) {
+                if (ok && mine > 0) job.warp_done(b, mine);   // the warp's results of batch b are stored
             }
             seg0 = seg1;
             b++;
