@@ -808,6 +808,9 @@ cudaError_t QG_CAT(expert_fused_, QG_NAME)(const ExpertArgs& a, int grid, cudaSt
     job.x = a.x;
     job.ids = a.ids;
     job.wts = a.wts;
+    // a routed call passes its routing outputs as ids / wts (the caller's writable buffers)
+    job.ids_out = a.route_kind >= 0 ? const_cast<int32_t*>(a.ids) : nullptr;
+    job.wts_out = a.route_kind >= 0 ? const_cast<float*>(a.wts) : nullptr;
     job.out = a.out;
     job.h = reinterpret_cast<float*>(a.ws + L.h);
     job.z = reinterpret_cast<float*>(a.ws + L.z);

@@ -38,7 +38,7 @@ struct HostMat {
 // Workspace of qexpert_group (all offsets 256-byte aligned):
 //   hdr      int32[8]     [0] status, [1] batches, [2] pairs (four-launch path);
 //                         [4..7] the one-launch path's counters (zero between calls)
-//   done     int32[256]   one-launch path: phase-A row tiles finished per batch (zero between calls)
+//   done     int32[kDoneWords]  one-launch path: phase-A row tiles finished per batch (zero between calls)
 //   batches  int4[P]      (expert, first sorted pair, pairs in batch, 0)
 //   pair_tok int32[P]     token of the sorted pair
 //   pair_of  int32[P]     sorted position of pair t * k + r
@@ -46,6 +46,7 @@ struct HostMat {
 //   h        f32[P][F]    silu(gate x) * (up x) of each sorted pair
 //   z        f32[P][D]    down h of each sorted pair
 constexpr int kMaxGrid = 1024;              // CTAs of an expert launch
+constexpr int kDoneWords = 256;             // per-batch counters of the one-launch path (its batches at most)
 struct WsLayout {
     size_t hdr, done, batches, pair_tok, pair_of, bounds, h, z, total;
 };
@@ -59,7 +60,7 @@ inline WsLayout ws_layout(int D, int F, int s, int k)
     WsLayout L;
     size_t off = 0;
     L.hdr = off;      off = align256(off + 8 * sizeof(int32_t));
-    L.done = off;     off = align256(off + 256 * sizeof(int32_t));
+    L.done = off;     off = align256(off + kDoneWords * sizeof(int32_t));
     L.batches = off;  off = align256(off + P * 4 * sizeof(int32_t));
     L.pair_tok = off; off = align256(off + P * sizeof(int32_t));
     L.pair_of = off;  off = align256(off + P * sizeof(int32_t));

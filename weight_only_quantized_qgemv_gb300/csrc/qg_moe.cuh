@@ -38,6 +38,7 @@
 
 constexpr int kMoeMaxPairs = 256;               // s * k of the fused launch
 static_assert(kMoeMaxPairs <= kTileThreads, "the prologue gives each thread at most one pair");
+static_assert(kMoeMaxPairs <= kDoneWords, "one workspace counter per batch");
 // pair tables: expert, weight, sorted position per pair; token, expert, batch
 // size per sorted position; first position per batch (+1); batches; flags
 constexpr int kMoeTabBytes = 6 * kMoeMaxPairs * 4 + (kMoeMaxPairs + 4) * 4 + kMoeMaxPairs * 16 + 64 * 4;
@@ -52,8 +53,10 @@ struct MoeJob {
     long long up_bytes, up_scales;  // bytes and scale elements of one gate / up matrix
     long long dn_bytes, dn_scales;  // of one down matrix
     const float* x;                 // [s][D]
-    const int32_t* ids;             // [s][k] (outputs when routed here)
+    const int32_t* ids;             // [s][k] (unused when routed here)
     const float* wts;
+    int32_t* ids_out;               // routed here: where CTA 0 writes the routing
+    float* wts_out;
     float* out;                     // [s][D]
     float* h;                       // workspace [P][F], by sorted pair position
     float* z;                       // workspace [P][D]
@@ -263,8 +266,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) k_moe(const __grid_constant__
                 s_exp[t * k + lane] = id;
                 s_w[t * k + lane] = w;
                 if (c == 0) {                      // one CTA writes the routing out
-                    const_cast<int32_t*>(job.ids)[t * k + lane] = id;
-                    const_cast<float*>(job.wts)[t * k + lane] = w;
+                    job.ids_out[t * k + lane] = id;
+                    job.wts_out[t * k + lane] = w;
                 }
             }
         }

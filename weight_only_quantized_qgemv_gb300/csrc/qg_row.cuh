@@ -329,132 +329,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_row(const __grid_constant__ 
     cp_async_wait<0>();
 }
 
-// The register-ring variant of the row-team kernel (one matrix, one
-// activation row, 16-byte chunks): each thread loads its chunk and scale of
-// the rows D steps ahead straight into registers (non-caching global loads),
-// with no shared-memory ring, so a chunk costs one load instead of a copy and
-// a read back.
-#ifndef QG_ROWL
-#define QG_ROWL 0
-#endif
-#ifndef QG_ROWL_RT
-#define QG_ROWL_RT 4
-#endif
-#ifndef QG_ROWL_D
-#define QG_ROWL_D 4
-#endif
-constexpr int kRowlRT = QG_ROWL_RT, kRowlD = QG_ROWL_D;
-
-__device__ __forceinline__ uint32_t ldg_u32(const void* p)
-{
-    uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-template <int F_, class Job>
-__global__ void __launch_bounds__(kRowThreads, 1) k_rowl(const __grid_constant__ Job job)
-{
-    constexpr int RT = kRowlRT, D = kRowlD;
-    constexpr int VS = pow2_ceil(RT * D);            // one round: the D steps in registers
-    const RowPlan& L = job.plan;
-    const int tid = threadIdx.x;
-    const bool active = tid < L.T;
-    const int g = tid / L.P, p = tid - g * L.P;
-    const int lane = tid & 31;
-
-    pdl_allow_next();
-    long long i0, i1;
-    job.cta_items(blockIdx.x, gridDim.x, i0, i1);
-    const long long G = L.G, GR = G * RT;
-    const long long first = i0 + (long long)g * RT;
-    const int n = (active && first < i1) ? (int)((i1 - first + GR - 1) / GR) : 0;
-
-    const uint8_t* cp[RT];
-    const uint8_t* sp[RT];
-#pragma unroll
-    for (int r = 0; r < RT; r++) {
-        const uint8_t* unused;
-        job.ptrs(0, n > 0 ? first + r : 0, p, cp[r], unused, sp[r]);
-    }
-    const long long cstep = GR * job.rb, sstep = GR * (long long)job.sbytes;
-    uint4 cw[D][RT];
-    [[maybe_unused]] uint32_t sw[D][RT];
-    long long irow = first;
-    int issued = 0;
-    auto load = [&](uint4 (&c)[RT], uint32_t (&sc)[RT]) {
-        if (issued < n) {
-#pragma unroll
-            for (int r = 0; r < RT; r++) {
-                if (irow + r < i1) {
-                    c[r] = ldg_stream16(cp[r]);
-                    if constexpr (SK != SK_ROW) sc[r] = ldg_u32(sp[r]);
-                }
-                cp[r] += cstep;
-                if constexpr (SK != SK_ROW) sp[r] += sstep;
-            }
-            irow += GR;
-        }
-        issued++;
-    };
-#pragma unroll
-    for (int v = 0; v < D; v++) load(cw[v], sw[v]);
-
-    pdl_wait_prev();                                 // activations and outputs from here on
-    float2 xr[EPL / 2];
-    {
-        const float4* src = reinterpret_cast<const float4*>(job.xrow(0) + (long long)p * EPL);
-#pragma unroll
-        for (int q = 0; q < EPL / 4; q++) {
-            const float4 f = active ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            xr[2 * q] = make_float2(f.x, f.y);
-            xr[2 * q + 1] = make_float2(f.z, f.w);
-        }
-    }
-    float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(qg_smem4) + L.red_off);
-    const int warp_global = tid >> 5;
-    int buf = 0;
-    for (int j0 = 0; j0 < n; j0 += D) {
-        float vb[VS];
-#pragma unroll
-        for (int i = 0; i < VS; i++) vb[i] = 0.f;
-#pragma unroll
-        for (int v = 0; v < D; v++) {
-            if (j0 + v < n) {
-#pragma unroll
-                for (int r = 0; r < RT; r++) {
-                    Chunk<F_> ch;
-                    ch.w = cw[v][r];
-                    const float dsum = chunk_dot<F_>(ch, xr);
-                    if constexpr (SK == SK_E8M0)
-                        vb[v * RT + r] = dsum * e8m0_to_f32(__byte_perm(sw[v][r], 0u, 0x4440u + (uint32_t)(p & 3)));
-                    else if constexpr (SK == SK_F32)
-                        vb[v * RT + r] = dsum * __uint_as_float(sw[v][r]);
-                    else
-                        vb[v * RT + r] = dsum;
-                }
-                load(cw[v], sw[v]);                  // the step D ahead into the registers just used
-            }
-        }
-        if (!active) continue;
-        const float rv = warp_reduce_scatter<VS>(vb, lane);
-        const int idx = reduce_scatter_index<VS>(lane);
-        float* rbuf = red + (size_t)buf * (kRowThreads / 32) * 16;
-        if (lane < VS) rbuf[warp_global * 16 + idx] = rv;
-        asm volatile("bar.sync %0, %1;" :: "r"(1 + g), "r"(L.P) : "memory");
-        if (p < RT * D) {
-            const int v = p / RT, r = p - v * RT;
-            const long long o = first + (long long)(j0 + v) * GR + r;
-            if (j0 + v < n && o < i1) {
-                float t = 0.f;
-                for (int w = 0; w < L.W; w++) t += rbuf[(g * L.W + w) * 16 + p];
-                job.store(0, o, SK == SK_ROW ? t * job.row_scale(0, o) : t);
-            }
-        }
-        buf ^= 1;
-    }
-}
-
 #ifndef QG_ROW
 #define QG_ROW 1
 #endif
@@ -505,13 +379,6 @@ static cudaError_t launch_row_dense(const DenseJob<NM>& dj, int grid, cudaStream
     job.rb = code_row_bytes(I);
     job.rbB = I / 8;
     job.sbytes = SK == SK_ROW ? 0 : (SK == SK_E8M0 ? dj.m[0].ngrp : 4 * dj.m[0].ngrp);
-    if constexpr (QG_ROWL && NM == 1 && S == 1 && FMT != FMT_INT3_G64) {
-        // the register ring needs only the reduction buffers in shared memory
-        static_assert(pow2_ceil(kRowlRT * kRowlD) <= 16, "reduction buffers hold 16 values per warp");
-        job.plan.red_off = 0;
-        job.plan.total = 2 * (kRowThreads / 32) * 16 * 4;
-        return launch_pdl(k_rowl<FMT, RowDenseJob<NM>>, dim3(grid), dim3(kRowThreads), (size_t)job.plan.total, st, job);
-    }
     auto kern = k_row<NM, S, RowDenseJob<NM>>;
     static int granted[64];
     cudaError_t e = set_smem(kern, (size_t)job.plan.total, granted);
