@@ -366,7 +366,10 @@ int qdevice_error(int clear);
  * QKERNEL_ROW the row-team kernel wherever its plan fits (one activation
  * row, rows a whole number of 32-chunk warp steps; else the automatic
  * choice).  The ring and tile kernels give the same bits; the
- * row-team kernel sums each row in another (fixed) order.  Returns the
+ * row-team kernel sums each row in another (fixed) order.  For the expert
+ * group, QKERNEL_AUTO and QKERNEL_ROW take the one-launch path where it
+ * applies, QKERNEL_RING and QKERNEL_TILE the four launches (the same bits
+ * as the one launch under QKERNEL_TILE).  Returns the
  * previous policy, or QSTATUS_BAD_FMT for an unknown one (the policy is then
  * unchanged).  Not synchronized with launches in flight on other threads.
  */
